@@ -1,0 +1,51 @@
+"""Plant plausible mistakes in copies of the oracle; the pins must catch each.
+
+Every mutant is a textual edit of oracle.c compiled into a temporary library
+on the CPU.  The product library is not involved.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pin_checks as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, original text, mutated text); each original must occur in oracle.c
+MUTANTS = [
+    ("bias_sign", "if (b) z += (double)b[n];", "if (b) z -= (double)b[n];"),
+    ("dropped_last_k", "for (int64_t k = 0; k < K; ++k) s += (double)x[k] * (double)w[k];",
+     "for (int64_t k = 0; k + 1 < K; ++k) s += (double)x[k] * (double)w[k];"),
+    ("gelu_scale", "erf(z / sqrt(2.0))", "erf(z / 2.0)"),
+    ("gelu_tanh_form", "return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));",
+     "return 0.5 * z * (1.0 + tanh(0.7978845608028654 * (z + 0.044715 * z * z * z)));"),
+    ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    ("bf16_7_bits", "ldexp(nearbyint(ldexp(m, 8)), e - 8)", "ldexp(nearbyint(ldexp(m, 7)), e - 7)"),
+    ("bf16_truncate", "ldexp(nearbyint(ldexp(m, 8)), e - 8)", "ldexp(floor(ldexp(m, 8)), e - 8)"),
+    ("column_shard_offset", "const float* Wi = W + (int64_t)i * ns * ldw;",
+     "const float* Wi = W + (int64_t)i * ns;"),
+    ("column_concat_offset", "double* Yi = Y + (int64_t)i * ns;", "double* Yi = Y;"),
+    ("row_input_slice", "int rc = orc_linear(M, ks, N, X + (int64_t)i * ks, ldx,",
+     "int rc = orc_linear(M, ks, N, X, ldx,"),
+    ("row_bias_per_shard", "W + (int64_t)i * ks, ldw, NULL, ORC_ACT_NONE, part, N);",
+     "W + (int64_t)i * ks, ldw, b, ORC_ACT_NONE, part, N);"),
+    ("qkv_kv_group", "(int64_t)H * hd + (int64_t)i * hk * hd,", "(int64_t)H * hd,"),
+    ("swiglu_swapped", "Y[m * ldy + n] = orc_silu(g) * u;", "Y[m * ldy + n] = orc_silu(u) * g;"),
+    ("h_not_rounded", "if (round_h) h[j] = orc_round_bf16(h[j]);", "(void)round_h;"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, orig, mut):
+    src = open(SRC).read()
+    assert orig in src, f"mutation site for {name} not found"
+    path = tmp_path / f"oracle_{name}.c"
+    path.write_text(src.replace(orig, mut, 1))
+    lib = tmp_path / f"liboracle_{name}.so"
+    subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+                    str(path), "-o", str(lib), "-lm"], check=True)
+    res = pins.run_all(oracle.Oracle(str(lib)))
+    failed = [k for k, v in res.items() if v is not None]
+    assert failed, f"mutant {name} passed every pin"
