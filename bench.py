@@ -1,0 +1,561 @@
+#!/usr/bin/env python3
+"""Benchmark: TP-sharded MLP block tokens/s on one B300, with its roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the path over one batch: the column-parallel linear with
+its fused activation, then the row-parallel linear with the in-kernel shard sum
+(exactly what tp_mlp_block launches), on synthetic seeded inputs of the
+workload's shapes.  Every tensor-parallel shard lives on the one GPU.  With
+--gpus N > 1 (under torchrun) each rank runs an independent replica: the path
+has no exchange between GPUs, so there is no collective on the data path; the
+barrier and the max-over-ranks timing are host bookkeeping.
+
+Printed (rank 0, one JSON line): whole-job tokens/s, the dominant kernel's
+achieved TFLOP/s or GB/s against the measured peak, the oracle's CPU
+throughput on a bounded sample, the end-to-end number through the public call
+with pinned host buffers, SM clocks sampled during the timed region.
+
+--impl reference times the fp64 CPU oracle (the plain implementation the
+tests check against) on the same workload, a bounded sample of rows per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TP-sharded MLP block tokens/s on 1 B300; % of HBM or bf16 tensor roofline"
+L2_BYTES = 126 * 1024 * 1024
+
+# name -> workload.  Shapes are the Llama-2-70B-sized layers (d_model 8192,
+# d_ff 28672; 64 query / 8 KV heads of dim 128) and the small GELU FFN block.
+WORKLOADS = {
+    "swiglu_ffn_prefill_tp8": dict(kind="ffn", M=4096, d=8192, dff=28672, tp=8, act="swiglu",
+                                   bias=False),
+    "swiglu_ffn_decode_tp4_b1": dict(kind="ffn", M=1, d=8192, dff=28672, tp=4, act="swiglu",
+                                     bias=False),
+    "swiglu_ffn_decode_tp4_b8": dict(kind="ffn", M=8, d=8192, dff=28672, tp=4, act="swiglu",
+                                     bias=False),
+    "swiglu_ffn_decode_tp4_b32": dict(kind="ffn", M=32, d=8192, dff=28672, tp=4, act="swiglu",
+                                      bias=False),
+    "swiglu_ffn_decode_tp4_b64": dict(kind="ffn", M=64, d=8192, dff=28672, tp=4, act="swiglu",
+                                      bias=False),
+    "gelu_ffn_tp2": dict(kind="ffn", M=16, d=512, dff=2048, tp=2, act="gelu", bias=True),
+    "attn_proj_tp8": dict(kind="attn", M=2048, d=8192, H=64, Hkv=8, hd=128, tp=8),
+}
+DEFAULT_WORKLOAD = "swiglu_ffn_prefill_tp8"
+
+
+# ------------------------------------------------------------------ work model
+def kernel_work(w):
+    """Algorithmic FLOPs and minimum HBM bytes of each kernel launch of one step.
+
+    bf16 operands (2 bytes), fp32 biases, bf16 intermediate h, bf16 output.
+    """
+    M, d = w["M"], w["d"]
+    if w["kind"] == "ffn":
+        dff = w["dff"]
+        n_w1 = 2 if w["act"] == "swiglu" else 1
+        col_flops = 2.0 * M * d * dff * n_w1
+        col_bytes = 2.0 * (n_w1 * dff * d + M * d + M * dff) + (4 * dff if w.get("bias") else 0)
+        row_flops = 2.0 * M * dff * d
+        row_bytes = 2.0 * (d * dff + M * dff + M * d) + (4 * d if w.get("bias") else 0)
+        return {"column": (col_flops, col_bytes), "row": (row_flops, row_bytes)}
+    H, Hkv, hd = w["H"], w["Hkv"], w["hd"]
+    nq = (H + 2 * Hkv) * hd
+    qkv_flops = 2.0 * M * d * nq
+    qkv_bytes = 2.0 * (nq * d + M * d + M * nq)
+    o_flops = 2.0 * M * H * hd * d
+    o_bytes = 2.0 * (d * H * hd + M * H * hd + M * d)
+    return {"column": (qkv_flops, qkv_bytes), "row": (o_flops, o_bytes)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                source="fallback")
+
+
+def traffic_record(workload):
+    """Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the
+    dominant kernel from the committed ncu summary -- only while the kernel's
+    source file still has the hash it had when the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return {}
+    if not rec:
+        return {}
+    try:
+        with open(os.path.join(ROOT, rec["source_file"]), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return {}
+    return rec if h == rec.get("source_sha256_16") else {}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """SM clock and clock-event (throttle) reasons of one GPU, polled through NVML
+    every `period_s` on a background thread while the timed region runs (reading
+    only: no setting is changed).  Works for timed regions of a few milliseconds."""
+
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake_slowdown", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.device_index = device_index
+        self.period_s = period_s
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.error = None
+        self._stop = None
+        self._thread = None
+
+    def _handle(self):
+        import pynvml
+        import torch
+        uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+        return pynvml.nvmlDeviceGetHandleByUUID(uuid)
+
+    def __enter__(self):
+        import threading
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = self._handle()
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # noqa: BLE001 - report, do not fail the benchmark
+            self.error = f"nvml unavailable: {type(e).__name__}"
+            return self
+        self._stop = threading.Event()
+
+        def poll():
+            masks = [(n, getattr(pynvml, a)) for n, a in self.REASONS]
+            while True:
+                try:
+                    self.samples.append(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
+                    r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+                    for n, m in masks:
+                        if r & m:
+                            self.reasons.add(n)
+                except Exception as e:  # noqa: BLE001
+                    self.error = f"nvml query failed: {type(e).__name__}"
+                    return
+                if self._stop.wait(self.period_s):
+                    return
+
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": [self.error or "no samples"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "nvml, polled every %g ms" % (self.period_s * 1e3)}
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_over_ranks(elapsed_ms: float, tokens: int, world: int):
+    """(max elapsed over ranks, total tokens over ranks).  Host bookkeeping only."""
+    if world <= 1:
+        return elapsed_ms, tokens
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ our arm
+class Path:
+    """Sharded weights on the device and the launches of one step."""
+
+    def __init__(self, w, device, seed=20_000):
+        import torch
+        from tensor_column_linear_gelu_b300 import inputs, tpla
+        self.w, self.tpla = w, tpla
+        tp = w["tp"]
+        if w["kind"] == "ffn":
+            f = inputs.ffn(seed, w["M"], w["d"], w["dff"], w["act"], w["bias"], device=device)
+            split = "gate_up" if w["act"] == "swiglu" else "column"
+            self.w1, self.b1 = tpla.tp_shard_weights(split, tp, f.W1, W_up=f.W_up, b=f.b1)
+            self.w2, _ = tpla.tp_shard_weights("row", tp, f.W2)
+            self.b2 = f.b2
+            self.X = f.X
+            self.h = torch.empty(w["M"], w["dff"], dtype=torch.bfloat16, device=device)
+            self.Y = torch.empty(w["M"], w["d"], dtype=torch.bfloat16, device=device)
+            del f
+        else:
+            a = inputs.attn(seed, w["M"], w["d"], w["H"], w["Hkv"], w["hd"], device=device)
+            heads = dict(n_heads=w["H"], n_kv_heads=w["Hkv"], head_dim=w["hd"])
+            self.w1, _ = tpla.tp_shard_weights("qkv_heads", tp, a.Wqkv, **heads)
+            self.w2, _ = tpla.tp_shard_weights("row", tp, a.Wo)
+            self.X, self.ctx = a.X, a.ctx
+            ws = (w["H"] // tp + 2 * (w["Hkv"] // tp)) * w["hd"]
+            self.qkv = torch.empty(tp, w["M"], ws, dtype=torch.bfloat16, device=device)
+            self.Y = torch.empty(w["M"], w["d"], dtype=torch.bfloat16, device=device)
+            del a
+        torch.cuda.synchronize()
+
+    # The FFN step as its two launches: exactly the sequence tp_mlp_block issues
+    # (column with fused activation into h, then row with the shard sum), so a
+    # CUDA event can sit between them.  The attention step is timed whole.
+    def parts(self):
+        w, t = self.w, self.tpla
+        if w["kind"] == "ffn":
+            def column(s):
+                t.column_parallel_linear(w["tp"], self.X, self.w1, self.b1, w["act"], Y=self.h,
+                                         N=w["dff"], stream=s)
+
+            def row(s):
+                t.row_parallel_linear(w["tp"], self.h, self.w2, self.b2, Y=self.Y, stream=s)
+            return [("column", column), ("row", row)]
+        return [("attn_proj", lambda s: self.step_public(s))]
+
+    def step_public(self, s, X=None, Y=None):
+        """One step through the public call a user makes."""
+        w, t = self.w, self.tpla
+        X = self.X if X is None else X
+        Y = self.Y if Y is None else Y
+        if w["kind"] == "ffn":
+            t.tp_mlp_block(w["tp"], X, self.w1, self.b1, self.w2, self.b2, w["act"],
+                           d_ff=w["dff"], h=self.h, Y=Y, stream=s)
+        else:
+            t.tp_attn_proj(w["tp"], X, self.w1, None, self.ctx, self.w2, None, w["H"], w["Hkv"],
+                           w["hd"], qkv_out=self.qkv, Y=Y, stream=s)
+
+    @staticmethod
+    def launches_per_step():
+        return 2
+
+
+def run_ours(args, w, rank, local_rank, world):
+    import torch
+    from tensor_column_linear_gelu_b300 import tpla
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    path = Path(w, dev)
+    s = torch.cuda.Stream(device=dev)
+    parts = path.parts()
+    work = kernel_work(w)
+    step_bytes = sum(b for _, b in work.values())
+    flush = None
+    if step_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            for _, fn in parts:
+                fn(s)
+    s.synchronize()
+    st = tpla.tp_device_status(s)
+    if st != tpla.TP_OK:
+        raise RuntimeError(f"device status after warm-up: {tpla.status_string(st)}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    with clocks:
+        with torch.cuda.stream(s):
+            for k in range(K):
+                if flush is not None:
+                    flush.zero_()          # evict L2 between steps (outside the step events)
+                ev[k][0].record(s)
+                for j, (_, fn) in enumerate(parts):
+                    fn(s)
+                    ev[k][j + 1].record(s)
+        s.synchronize()
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    st = tpla.tp_device_status(s)
+    if st != tpla.TP_OK:
+        raise RuntimeError(f"device status after timed region: {tpla.status_string(st)}")
+
+    per_part = {name: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)]
+                for j, (name, _) in enumerate(parts)}
+    step_ms = [ev[k][0].elapsed_time(ev[k][len(parts)]) for k in range(K)]
+    # Steps run back to back: with no flush the span first->last event is the
+    # timed region on the device; with a flush the flushes are excluded.
+    if flush is None:
+        elapsed_ms = ev[0][0].elapsed_time(ev[K - 1][len(parts)])
+    else:
+        elapsed_ms = sum(step_ms)
+    tokens_local = w["M"] * K
+    elapsed_max, tokens_all = reduce_over_ranks(elapsed_ms, tokens_local, world)
+
+    # ---------------------------------------------------------- roofline
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if w["kind"] == "ffn":
+        avg = {n: sum(v) / len(v) for n, v in per_part.items()}
+        dom = max(avg, key=avg.get)
+        flops, nbytes = work[dom]
+        dur_s = avg[dom] / 1e3
+        launches_in_dom = 1
+    else:
+        dom = "attn_proj"
+        flops = sum(f for f, _ in work.values())
+        nbytes = sum(b for _, b in work.values())
+        dur_s = (sum(per_part["attn_proj"]) / K) / 1e3
+        launches_in_dom = 2
+    bound = "tensor" if flops / nbytes > ridge else "hbm"
+    long_region = elapsed_ms > 1000.0
+    if bound == "tensor":
+        peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+        achieved = flops / dur_s / 1e12
+        unit = "TFLOP/s"
+        peak_kind = ("sustained" if long_region else "burst") + " bf16, " + peaks["source"]
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = nbytes / dur_s / 1e9
+        unit = "GB/s"
+        peak_kind = "hbm copy, " + peaks["source"]
+    tr = traffic_record(args.workload)
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": tr.get("bytes_per_launch"),
+                "kernel": dom, "launches": launches_in_dom,
+                "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+                "avg_ms": round(dur_s * 1e3, 4), "peak_kind": peak_kind}
+    if tr.get("bytes_per_launch") is not None:
+        roofline["traffic_source"] = tr.get("source")
+
+    e2e = run_e2e(path, w, s, args)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, budget_s=args.cpu_seconds)
+
+    return dict(elapsed_max=elapsed_max, tokens_all=tokens_all, roofline=roofline,
+                per_part={n: round(sum(v) / len(v), 4) for n, v in per_part.items()},
+                clocks=clocks.summary(), e2e=e2e, cpu=cpu, flush=flush is not None,
+                launches=K * path.launches_per_step())
+
+
+def run_e2e(path, w, s, args):
+    """Same metric through the public call, with the step's input copied in from
+    pinned host memory and the result read back to pinned host memory, every step."""
+    import torch
+    Xh = path.X.to("cpu").pin_memory()
+    Yh = torch.empty(path.Y.shape, dtype=path.Y.dtype).pin_memory()
+    Xd = torch.empty_like(path.X)
+    Yd = torch.empty_like(path.Y)
+    K = args.steps
+    with torch.cuda.stream(s):
+        for _ in range(max(1, args.warmup)):
+            Xd.copy_(Xh, non_blocking=True)
+            path.step_public(s, Xd, Yd)
+            Yh.copy_(Yd, non_blocking=True)
+    s.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(K):
+            Xd.copy_(Xh, non_blocking=True)
+            path.step_public(s, Xd, Yd)
+            Yh.copy_(Yd, non_blocking=True)
+        e1.record(s)
+    s.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(w["M"] * K / (ms / 1e3), 2), "unit": "tokens/s",
+            "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
+            "d2h_bytes_per_step": Yh.numel() * Yh.element_size(),
+            "ms_per_step": round(ms / K, 4)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_inputs(w, rows, seed=20_000):
+    """Host float32 inputs the oracle needs for `rows` sampled rows of the workload
+    (the same seeded tensors the GPU arm uses)."""
+    import torch
+    from tensor_column_linear_gelu_b300 import inputs
+    dev = "cuda" if torch.cuda.is_available() else None
+    if w["kind"] == "ffn":
+        f = inputs.ffn(seed, w["M"], w["d"], w["dff"], w["act"], w["bias"], device=dev)
+        a = dict(X=f.X[rows].float().cpu().numpy(), W1=f.W1.float().cpu().numpy(),
+                 W1u=None if f.W_up is None else f.W_up.float().cpu().numpy(),
+                 W2=f.W2.float().cpu().numpy(),
+                 b1=None if f.b1 is None else f.b1.cpu().numpy(),
+                 b2=None if f.b2 is None else f.b2.cpu().numpy())
+        del f
+        return a
+    at = inputs.attn(seed, w["M"], w["d"], w["H"], w["Hkv"], w["hd"], device=dev)
+    a = dict(X=at.X[rows].float().cpu().numpy(), Wqkv=at.Wqkv.float().cpu().numpy(),
+             ctx=at.ctx[rows].float().cpu().numpy(), Wo=at.Wo.float().cpu().numpy())
+    del at
+    return a
+
+
+def oracle_step(orc, w, a):
+    if w["kind"] == "ffn":
+        orc.mlp_block(w["tp"], a["X"], a["W1"], a["b1"], a["W2"], a["b2"], w["act"], W1u=a["W1u"],
+                      round_h=True)
+    else:
+        orc.qkv_proj(w["tp"], a["X"], a["Wqkv"], None, w["H"], w["Hkv"], w["hd"])
+        orc.o_proj(w["tp"], a["ctx"], a["Wo"], None, w["H"], w["hd"])
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """The oracle, as it stands, on a bounded sample of the workload's rows."""
+    import oracle
+    from tensor_column_linear_gelu_b300 import inputs
+    orc = oracle.default()
+    rows = inputs.sample_rows(w["M"], 1, 20_000)
+    a = oracle_inputs(w, rows)
+    t0 = time.perf_counter()
+    oracle_step(orc, w, a)
+    t1 = time.perf_counter() - t0
+    n = int(max(1, min(w["M"], math.floor(budget_s / max(t1, 1e-3)))))
+    if n > 1:
+        rows = inputs.sample_rows(w["M"], n, 20_000)
+        a = oracle_inputs(w, rows)
+        t0 = time.perf_counter()
+        oracle_step(orc, w, a)
+        t1 = time.perf_counter() - t0
+    n = len(rows)
+    return {"value": round(n / t1, 4), "unit": "tokens/s", "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} of {w['M']} rows of the same workload (fp64 C oracle, OpenMP), "
+                      f"{t1:.1f} s"}
+
+
+def run_reference(args, w, rank, world):
+    """--impl reference: the oracle on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return None
+    import oracle
+    from tensor_column_linear_gelu_b300 import inputs
+    orc = oracle.default()
+    rows_per_step = max(1, min(w["M"], args.ref_rows))
+    rows = inputs.sample_rows(w["M"], rows_per_step, 20_000)
+    a = oracle_inputs(w, rows)
+    for _ in range(args.warmup):
+        oracle_step(orc, w, a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(orc, w, a)
+    el = time.perf_counter() - t0
+    value = rows_per_step * args.steps / el
+    sample = f"{rows_per_step} of {w['M']} rows per step (fp64 C oracle, OpenMP)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(args.workload, w, world),
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s",
+                             "cores": orc.num_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def workload_config(name, w, world):
+    c = {"workload": name}
+    c.update({k: v for k, v in w.items() if k != "kind"})
+    c["parallelism"] = f"tp{w['tp']} simulated on 1 GPU" + (f", {world} replicas" if world > 1 else "")
+    return c
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+
+    if args.impl == "reference":
+        out = run_reference(args, w, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    r = run_ours(args, w, rank, local_rank, world)
+    if rank == 0:
+        K = args.steps
+        value = r["tokens_all"] / (r["elapsed_max"] / 1e3)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(r["elapsed_max"] / K, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(workload_config(args.workload, w, world),
+                           l2=("L2 flushed between steps (256 MB write)" if r["flush"] else
+                               "inputs larger than L2 (weights stream from HBM every step)")),
+            "roofline": r["roofline"], "cpu_baseline": r["cpu"], "e2e": r["e2e"],
+            "gpu_launches": r["launches"], "clocks": r["clocks"],
+            "kernel_ms": r["per_part"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,303 @@
+/*
+ * tpla.h -- tensor-parallel linear algebra on one GPU (B300, sm_103a).
+ *
+ * The Megatron-style split of a transformer layer's linear algebra, with every
+ * tensor-parallel shard materialised on ONE device and the all-reduce's sum
+ * done inside the kernel:
+ *
+ *   column-parallel linear   Y_i = act(X . W_i^T + b_i)   (W split on outputs)
+ *   row-parallel linear      Y   = sum_i X_i . W_i^T + b  (W split on inputs,
+ *                                                           bias added once)
+ *   FFN block                column -> act per shard -> row
+ *   attention projections    QKV column-split by head group, O row-split by
+ *                            head
+ *
+ * Sources (page title -- section):
+ *   [P3] "Understanding Tensor Parallelism for Multi-GPU LLM Serving" --
+ *        "How Tensor Parallelism Works Under the Hood" and the
+ *        ColumnParallelLinear / RowParallelLinear modules of "Implementing
+ *        Tensor Parallelism with Hugging Face Accelerate".
+ *   [P4] "What is tensor parallelism?" -- "How a layer is split", "Why it
+ *        helps when serving".
+ *   [P5] "Tensor parallel serving" -- "Simulating the split, and proving it is
+ *        correct", "Column-parallel and row-parallel layers, paired".
+ *
+ * Conventions shared by every entry point
+ *   - Weights are stored like nn.Linear: [out_features, in_features],
+ *     row-major.  Activations are row-major [tokens, features].
+ *   - Every data pointer is DEVICE memory owned by the caller; host arrays of
+ *     shard pointers (w_shards, b_shards) are read during the call only.  The
+ *     library never allocates, frees or retains caller memory.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream).  Outputs must not alias inputs.
+ *   - Arguments are validated before anything is launched.  On any error the
+ *     call returns a status, writes nothing and launches nothing.  No C++
+ *     exception crosses this boundary.
+ *   - Alignment: X, weight shards and the FFN workspace are 16-byte aligned,
+ *     and every input row stride (ld * element size) and weight row length
+ *     (in_features * element size, per shard) is a multiple of 16 bytes, as
+ *     128-bit and TMA loads need.  Outputs and biases need only their natural
+ *     alignment.  Otherwise TP_ERR_ALIGNMENT.
+ *   - 1 <= tp <= TP_MAX_TP.  tp = 1 is the unsharded layer.
+ *   - M = 0 (no tokens) is a valid empty call: TP_OK, nothing launched.
+ *   - Arithmetic: bf16 inputs are multiplied exactly and accumulated in fp32;
+ *     bias, activation and the shard sum are fp32; the result is rounded once
+ *     to the output dtype (round to nearest even for bf16).  fp32 inputs use
+ *     fp32 FMA on CUDA cores (no TF32).
+ *   - Determinism: the summation order of a column-parallel output depends
+ *     only on (M, K, dtype, act), never on N or tp, so a sharded run is
+ *     bit-identical to the same call with tp = 1.
+ */
+#ifndef TPLA_H
+#define TPLA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the same underlying type). */
+typedef struct CUstream_st* tp_stream_t;
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_NULL = 1,            /* a required pointer is NULL */
+  TP_ERR_NOT_DIVISIBLE = 2,   /* tp does not divide a split dimension */
+  TP_ERR_BAD_SHAPE = 3,       /* negative/zero size, tp out of range, ld too small */
+  TP_ERR_DTYPE = 4,           /* unsupported dtype combination */
+  TP_ERR_ALIGNMENT = 5,       /* pointer or stride not 16-byte aligned */
+  TP_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed */
+  TP_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device-side wait gave up */
+  TP_ERR_UNSUPPORTED = 8      /* valid but not offered (e.g. a bias where none is defined) */
+} tp_status;
+
+typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
+
+typedef enum {
+  TP_ACT_NONE = 0,
+  TP_ACT_GELU_ERF = 1, /* 0.5 z (1 + erf(z / sqrt 2)), the torch F.gelu default */
+  TP_ACT_SWIGLU = 2    /* silu(x.Wg^T) * (x.Wu^T); packed gate/up shards, no bias */
+} tp_act;
+
+typedef enum {
+  TP_SPLIT_COLUMN = 0,    /* rows [i*out/tp, (i+1)*out/tp) of W  -> [out/tp, in]  */
+  TP_SPLIT_ROW = 1,       /* cols [i*in/tp,  (i+1)*in/tp)  of W  -> [out, in/tp]  */
+  TP_SPLIT_QKV_HEADS = 2, /* head group i of a [Q;K;V] weight    -> [(H+2Hkv)/tp*hd, in] */
+  TP_SPLIT_GATE_UP = 3    /* gate/up rows of shard i, packed     -> [2*G*ceil(out/tp/G), in] */
+} tp_split;
+
+/* Largest tensor-parallel size accepted. */
+#define TP_MAX_TP 16
+
+/*
+ * Row-group size G of a packed gate/up (SwiGLU) shard.  Packed shard i holds,
+ * for each group j = 0, 1, ...: gate rows i*out/tp + j*G + [0, G) followed by
+ * up rows i*out/tp + j*G + [0, G).  Rows past out/tp in the last group are
+ * zero.  One GEMM tile therefore holds matching gate and up outputs.
+ */
+#define TP_GATE_UP_GROUP 128
+
+/* Human-readable name of a status; never NULL. */
+const char* tp_status_string(tp_status status);
+
+/*
+ * tp_shard_shape -- rows and columns of one weight shard produced by
+ * tp_shard_weights for this split.
+ *
+ * Defined by the shard shapes of ColumnParallelLinear ([out/tp, in]) and
+ * RowParallelLinear ([out, in/tp]) in [P3], the head split of [P4], and the
+ * gate/up packing above.  out_f/in_f are the unsharded weight's dimensions;
+ * n_heads, n_kv_heads, head_dim are read for TP_SPLIT_QKV_HEADS only (then
+ * out_f must equal (n_heads + 2*n_kv_heads) * head_dim).
+ * Errors: TP_ERR_NULL (rows or cols NULL), TP_ERR_BAD_SHAPE, TP_ERR_NOT_DIVISIBLE.
+ */
+tp_status tp_shard_shape(tp_split split, int tp, int64_t out_f, int64_t in_f,
+                         int n_heads, int n_kv_heads, int head_dim,
+                         int64_t* rows, int64_t* cols);
+
+/*
+ * tp_shard_weights -- cut an unsharded weight (and bias) into tp contiguous
+ * shards on the device.  A bit-preserving copy; one-time setup.
+ *
+ * [P3] ColumnParallelLinear / RowParallelLinear (shard shapes, the asserts
+ * out_features % tp == 0 and in_features % tp == 0); [P5] "Simulating the
+ * split" (W[:split], W[split:] and b likewise); [P4] (heads to different
+ * GPUs; tp divides the head count).
+ *
+ *   split        which cut (tp_split).
+ *   wdt          element type of W, W_up and the shards (TP_F32 or TP_BF16).
+ *   W            [out_f, in_f] unsharded weight (gate weight for GATE_UP),
+ *                device memory.
+ *   W_up         [out_f, in_f] up weight for TP_SPLIT_GATE_UP, else NULL.
+ *   b            fp32 [out_f] bias or NULL.  Sharded for COLUMN and
+ *                QKV_HEADS.  ROW and GATE_UP take no bias here
+ *                (TP_ERR_UNSUPPORTED): a row-parallel bias is added once,
+ *                after the shard sum, and is passed whole to
+ *                row_parallel_linear.
+ *   n_heads, n_kv_heads, head_dim   QKV_HEADS only; W's rows are
+ *                [Q heads 0..H-1; K heads 0..Hkv-1; V heads 0..Hkv-1], each
+ *                head_dim rows.  Shard i gets Q heads [i*H/tp, (i+1)*H/tp),
+ *                then K and V heads [i*Hkv/tp, (i+1)*Hkv/tp).
+ *   w_shards     host array of tp device pointers, each to a buffer of
+ *                tp_shard_shape() rows x cols elements (row-major, contiguous).
+ *   b_shards     host array of tp device pointers to fp32 [rows] buffers, or
+ *                NULL; required exactly when b is given.
+ * Errors: TP_ERR_NULL, TP_ERR_BAD_SHAPE, TP_ERR_NOT_DIVISIBLE (tp must divide
+ * out_f, in_f, H or Hkv as the split needs), TP_ERR_ALIGNMENT, TP_ERR_DTYPE,
+ * TP_ERR_UNSUPPORTED, TP_ERR_CUDA.
+ */
+tp_status tp_shard_weights(tp_split split, int tp, tp_dtype wdt, const void* W,
+                           const void* W_up, int64_t out_f, int64_t in_f,
+                           const float* b, int n_heads, int n_kv_heads,
+                           int head_dim, void* const* w_shards,
+                           float* const* b_shards, tp_stream_t stream);
+
+/*
+ * column_parallel_linear -- Y_i = act(X . W_i^T + b_i) for every shard i, in
+ * one launch; shard i writes columns [i*N/tp, (i+1)*N/tp) of Y, so the
+ * concatenation of [P5] is the output layout itself.
+ *
+ * [P3] "How Tensor Parallelism Works Under the Hood" (column parallelism: the
+ * full input X is shared, each shard computes a slice of the output) and
+ * ColumnParallelLinear.forward; the nonlinearity applied per shard follows
+ * the FFN demo of [P3] (h = gelu(ffn_up(x))).
+ *
+ *   M, K, N      tokens, input features, output features of the UNSHARDED
+ *                layer (N % tp == 0).
+ *   X            [M, K] (row stride ldx >= K), dtype xdt.
+ *   w_shards     host array of tp device pointers; shard i is [N/tp, K]
+ *                (TP_SPLIT_COLUMN) or, for TP_ACT_SWIGLU, the packed gate/up
+ *                shard of TP_SPLIT_GATE_UP.  Same dtype as X.
+ *   b_shards     host array of tp fp32 [N/tp] device pointers, or NULL for
+ *                no bias.  Must be NULL for TP_ACT_SWIGLU.
+ *   act          TP_ACT_NONE, TP_ACT_GELU_ERF or TP_ACT_SWIGLU.
+ *   Y            [M, N] (row stride ldy >= N), dtype ydt.
+ *   xdt / ydt    TP_BF16 in with TP_BF16 or TP_F32 out; TP_F32 in with
+ *                TP_F32 out.
+ * Errors: TP_ERR_NULL, TP_ERR_BAD_SHAPE, TP_ERR_NOT_DIVISIBLE, TP_ERR_DTYPE,
+ * TP_ERR_ALIGNMENT, TP_ERR_UNSUPPORTED, TP_ERR_CUDA.
+ */
+tp_status column_parallel_linear(int tp, int64_t M, int64_t K, int64_t N,
+                                 const void* X, int64_t ldx, tp_dtype xdt,
+                                 const void* const* w_shards,
+                                 const float* const* b_shards, tp_act act,
+                                 void* Y, int64_t ldy, tp_dtype ydt,
+                                 tp_stream_t stream);
+
+/*
+ * row_parallel_linear -- Y = sum_{i=0}^{tp-1} X_i . W_i^T + b, one fp32
+ * accumulator walking the shards in order 0..tp-1, the bias added once after
+ * the sum.  This is the all-reduce's arithmetic, done inside the kernel.
+ *
+ * [P3] "How Tensor Parallelism Works Under the Hood" (row parallelism: each
+ * shard computes a partial sum, an all-reduce adds them) and
+ * RowParallelLinear.forward (all_reduce SUM, then + bias); [P5] (sum, not
+ * concatenate).  X_i is the shard-local input, i.e. columns
+ * [i*K/tp, (i+1)*K/tp) of X (the output of the preceding column-parallel
+ * layer needs no re-slicing).
+ *
+ *   M, K, N      tokens, input features, output features of the UNSHARDED
+ *                layer (K % tp == 0).
+ *   X            [M, K] (row stride ldx >= K), dtype xdt.
+ *   w_shards     host array of tp device pointers; shard i is [N, K/tp]
+ *                (TP_SPLIT_ROW), same dtype as X.
+ *   b            fp32 [N] or NULL.
+ *   Y            [M, N] (row stride ldy >= N), dtype ydt.
+ * Errors: as column_parallel_linear.
+ */
+tp_status row_parallel_linear(int tp, int64_t M, int64_t K, int64_t N,
+                              const void* X, int64_t ldx, tp_dtype xdt,
+                              const void* const* w_shards, const float* b,
+                              void* Y, int64_t ldy, tp_dtype ydt,
+                              tp_stream_t stream);
+
+/*
+ * tp_mlp_block -- the tensor-parallel FFN block: column-parallel first linear
+ * with the activation applied per shard, then row-parallel second linear whose
+ * shard-i input is h_i, summed in the kernel, + b2 once.
+ *
+ * [P3] "How Tensor Parallelism Works Under the Hood" (the first FFN linear is
+ * column-parallel, the second row-parallel, one synchronisation per block)
+ * and its FFN demo; [P5] "Column-parallel and row-parallel layers, paired"
+ * (the intermediate activation is never exchanged).
+ *
+ *   d_model, d_ff  layer widths; d_ff % tp == 0.
+ *   act          TP_ACT_GELU_ERF (w1 shards from TP_SPLIT_COLUMN, optional
+ *                b1 shards) or TP_ACT_SWIGLU (w1 shards from
+ *                TP_SPLIT_GATE_UP, b1 must be NULL) or TP_ACT_NONE.
+ *   X            [M, d_model] contiguous, dtype xdt.
+ *   w2_shards    shard i is [d_model, d_ff/tp] (TP_SPLIT_ROW).
+ *   b2           fp32 [d_model] or NULL.
+ *   h            caller-provided workspace [M, d_ff] contiguous, dtype xdt
+ *                (bf16 for bf16 inputs: the intermediate is stored in bf16).
+ *                On return (stream order) it holds the activation.
+ *   Y            [M, d_model] contiguous, dtype ydt.
+ * Errors: as column_parallel_linear.
+ */
+tp_status tp_mlp_block(int tp, int64_t M, int64_t d_model, int64_t d_ff,
+                       tp_act act, tp_dtype xdt, const void* X,
+                       const void* const* w1_shards,
+                       const float* const* b1_shards,
+                       const void* const* w2_shards, const float* b2, void* h,
+                       void* Y, tp_dtype ydt, tp_stream_t stream);
+
+/*
+ * tp_attn_proj -- the head-split attention projections: QKV column-parallel
+ * by head group, O row-parallel by head with the shard sum in the kernel.
+ * The attention core between them is not part of this call: ctx, the
+ * attention output [M, n_heads*head_dim], is an input.
+ *
+ * [P4] "How a layer is split" (different attention heads go to different
+ * GPUs) and "Why it helps when serving" (tp divides the head count); [P3]
+ * "What Is Tensor Parallelism?" (one exchange after the attention
+ * concatenation); [P5] "Column-parallel and row-parallel layers, paired" (one
+ * all-reduce per attention block).
+ *
+ *   n_heads, n_kv_heads, head_dim   tp divides both head counts.
+ *   X            [M, d_model] contiguous, dtype xdt.
+ *   wqkv_shards  shard i from TP_SPLIT_QKV_HEADS: [(H+2Hkv)/tp*hd, d_model].
+ *   bqkv_shards  host array of tp fp32 device pointers, or NULL.
+ *   qkv_out      [tp][M][(H+2Hkv)/tp*hd] shard-major (what device i would
+ *                hold: its Q heads, then its K head(s), then its V head(s)),
+ *                dtype qkv_dt.
+ *   ctx          [M, H*hd] contiguous, dtype xdt; shard i reads head columns
+ *                [i*H/tp*hd, (i+1)*H/tp*hd).
+ *   wo_shards    shard i from TP_SPLIT_ROW of W_o [d_model, H*hd]:
+ *                [d_model, H/tp*hd].
+ *   bo           fp32 [d_model] or NULL.
+ *   Y            [M, d_model] contiguous, dtype ydt.
+ * Errors: as column_parallel_linear.
+ */
+tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads,
+                       int n_kv_heads, int head_dim, tp_dtype xdt,
+                       const void* X, const void* const* wqkv_shards,
+                       const float* const* bqkv_shards, void* qkv_out,
+                       tp_dtype qkv_dt, const void* ctx,
+                       const void* const* wo_shards, const float* bo, void* Y,
+                       tp_dtype ydt, tp_stream_t stream);
+
+/*
+ * tp_device_status -- synchronise `stream`, then report and clear the
+ * library's device-side error word on the current device.  Every spin-wait
+ * inside the library's kernels is bounded; a wait that runs out sets this
+ * word and the kernel returns early (its output is then incomplete).
+ * Returns TP_OK, TP_ERR_DEVICE_TIMEOUT, or TP_ERR_CUDA if the stream itself
+ * reports an error.
+ */
+tp_status tp_device_status(tp_stream_t stream);
+
+/*
+ * tp_selftest_bounded_wait -- exercise the bounded-wait path: launch one
+ * kernel that waits on a barrier nothing will ever complete, with a limit of
+ * `limit_ns` nanoseconds (1 .. 10^10).  The kernel gives up, sets the device
+ * error word and returns; tp_device_status then reports
+ * TP_ERR_DEVICE_TIMEOUT and the context stays usable.  For tests.
+ */
+tp_status tp_selftest_bounded_wait(int64_t limit_ns, tp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPLA_H */

@@ -1,0 +1,351 @@
+// api.cu -- the C-ABI entry points of include/tpla.h: argument validation
+// (before any launch; on error nothing is written) and kernel dispatch.
+//
+// Dispatch keys on (M, K, dtype, act) only -- never on N or tp -- so a
+// column-parallel call computes every output with the same kernel and the
+// same summation order whatever the shard count.
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+
+namespace tpla {
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  if (dev >= 64) dev = 63;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+#define TP_RET_IF(cond, code) \
+  do {                        \
+    if (cond) return (code);  \
+  } while (0)
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al_to(const void* p, int64_t a) { return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)a) == 0; }
+int64_t esz(int dt) { return dt == TP_F32 ? 4 : 2; }
+bool valid_dtype(int dt) { return dt == TP_F32 || dt == TP_BF16; }
+// bf16 in -> bf16 or fp32 out; fp32 in -> fp32 out.
+bool valid_io(int xdt, int ydt) {
+  return valid_dtype(xdt) && valid_dtype(ydt) && !(xdt == TP_F32 && ydt == TP_BF16);
+}
+bool valid_act(int a) { return a == TP_ACT_NONE || a == TP_ACT_GELU_ERF || a == TP_ACT_SWIGLU; }
+bool valid_tp(int tp) { return tp >= 1 && tp <= TP_MAX_TP; }
+
+int64_t gate_up_rows(int64_t ns) {
+  const int64_t G = TP_GATE_UP_GROUP;
+  return 2 * G * ((ns + G - 1) / G);
+}
+
+tp_status check_ptr_array(const void* const* a, int tp) {
+  TP_RET_IF(!a, TP_ERR_NULL);
+  for (int i = 0; i < tp; ++i) TP_RET_IF(!a[i], TP_ERR_NULL);
+  return TP_OK;
+}
+
+tp_status check_aligned_array(const void* const* a, int tp) {
+  for (int i = 0; i < tp; ++i) TP_RET_IF(!al16(a[i]), TP_ERR_ALIGNMENT);
+  return TP_OK;
+}
+
+tp_status check_bias_array(const float* const* b, int tp) {
+  if (!b) return TP_OK;
+  for (int i = 0; i < tp; ++i) {
+    TP_RET_IF(!b[i], TP_ERR_NULL);
+    TP_RET_IF(!al_to(b[i], 4), TP_ERR_ALIGNMENT);
+  }
+  return TP_OK;
+}
+
+// The one place a validated problem picks its kernel.
+tp_status run(const LinearProblem& p, cudaStream_t s) {
+  if (p.M == 0) return TP_OK;
+  if (p.xdt == TP_BF16 && gemm_tc_supports(p)) return launch_gemm_tc(p, s);
+  return launch_gemv(p, s);
+}
+
+LinearProblem column_problem(int tp, int64_t M, int64_t K, int64_t N, const void* X,
+                             int64_t ldx, int xdt, const void* const* w,
+                             const float* const* b, int act, void* Y, int64_t ldy,
+                             int ydt, int64_t y_shard_stride) {
+  LinearProblem p;
+  p.tp = tp;
+  p.row = false;
+  p.act = act;
+  p.xdt = xdt;
+  p.ydt = ydt;
+  p.M = M;
+  p.K = K;
+  p.n_out = N;
+  p.ns = N / tp;
+  p.w_rows = (act == TP_ACT_SWIGLU) ? gate_up_rows(p.ns) : p.ns;
+  p.X = X;
+  p.ldx = ldx;
+  p.Y = Y;
+  p.ldy = ldy;
+  p.y_shard_stride = y_shard_stride;
+  for (int i = 0; i < tp; ++i) {
+    p.W[i] = w[i];
+    p.bias[i] = b ? b[i] : nullptr;
+  }
+  return p;
+}
+
+LinearProblem row_problem(int tp, int64_t M, int64_t K, int64_t N, const void* X, int64_t ldx,
+                          int xdt, const void* const* w, const float* b, void* Y, int64_t ldy,
+                          int ydt) {
+  LinearProblem p;
+  p.tp = tp;
+  p.row = true;
+  p.act = TP_ACT_NONE;
+  p.xdt = xdt;
+  p.ydt = ydt;
+  p.M = M;
+  p.K = K / tp;
+  p.n_out = N;
+  p.ns = N;
+  p.w_rows = N;
+  p.X = X;
+  p.ldx = ldx;
+  p.x_shard_off = K / tp;
+  p.Y = Y;
+  p.ldy = ldy;
+  for (int i = 0; i < tp; ++i) p.W[i] = w[i];
+  p.bias[0] = b;
+  return p;
+}
+
+}  // namespace
+}  // namespace tpla
+
+using namespace tpla;
+
+extern "C" {
+
+const char* tp_status_string(tp_status s) {
+  switch (s) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_NULL: return "TP_ERR_NULL: a required pointer is NULL";
+    case TP_ERR_NOT_DIVISIBLE: return "TP_ERR_NOT_DIVISIBLE: tp does not divide a split dimension";
+    case TP_ERR_BAD_SHAPE: return "TP_ERR_BAD_SHAPE: invalid size, tp or leading dimension";
+    case TP_ERR_DTYPE: return "TP_ERR_DTYPE: unsupported dtype combination";
+    case TP_ERR_ALIGNMENT: return "TP_ERR_ALIGNMENT: pointer or stride not 16-byte aligned";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA: a CUDA call failed";
+    case TP_ERR_DEVICE_TIMEOUT: return "TP_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED: argument combination not offered";
+  }
+  return "unknown tp_status";
+}
+
+tp_status tp_shard_shape(tp_split split, int tp, int64_t out_f, int64_t in_f, int n_heads,
+                         int n_kv_heads, int head_dim, int64_t* rows, int64_t* cols) {
+  TP_RET_IF(!rows || !cols, TP_ERR_NULL);
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(out_f <= 0 || in_f <= 0, TP_ERR_BAD_SHAPE);
+  switch (split) {
+    case TP_SPLIT_COLUMN:
+      TP_RET_IF(out_f % tp, TP_ERR_NOT_DIVISIBLE);
+      *rows = out_f / tp;
+      *cols = in_f;
+      return TP_OK;
+    case TP_SPLIT_ROW:
+      TP_RET_IF(in_f % tp, TP_ERR_NOT_DIVISIBLE);
+      *rows = out_f;
+      *cols = in_f / tp;
+      return TP_OK;
+    case TP_SPLIT_QKV_HEADS:
+      TP_RET_IF(n_heads < 1 || n_kv_heads < 1 || head_dim < 1, TP_ERR_BAD_SHAPE);
+      TP_RET_IF(out_f != (int64_t)(n_heads + 2 * (int64_t)n_kv_heads) * head_dim,
+                TP_ERR_BAD_SHAPE);
+      TP_RET_IF(n_heads % tp || n_kv_heads % tp, TP_ERR_NOT_DIVISIBLE);
+      *rows = (int64_t)(n_heads / tp + 2 * (n_kv_heads / tp)) * head_dim;
+      *cols = in_f;
+      return TP_OK;
+    case TP_SPLIT_GATE_UP:
+      TP_RET_IF(out_f % tp, TP_ERR_NOT_DIVISIBLE);
+      *rows = gate_up_rows(out_f / tp);
+      *cols = in_f;
+      return TP_OK;
+  }
+  return TP_ERR_BAD_SHAPE;
+}
+
+tp_status tp_shard_weights(tp_split split, int tp, tp_dtype wdt, const void* W, const void* W_up,
+                           int64_t out_f, int64_t in_f, const float* b, int n_heads,
+                           int n_kv_heads, int head_dim, void* const* w_shards,
+                           float* const* b_shards, tp_stream_t stream) {
+  int64_t rows = 0, cols = 0;
+  tp_status st = tp_shard_shape(split, tp, out_f, in_f, n_heads, n_kv_heads, head_dim, &rows, &cols);
+  if (st != TP_OK) return st;
+  TP_RET_IF(!valid_dtype(wdt), TP_ERR_DTYPE);
+  TP_RET_IF(b && split != TP_SPLIT_COLUMN && split != TP_SPLIT_QKV_HEADS, TP_ERR_UNSUPPORTED);
+  TP_RET_IF(!W, TP_ERR_NULL);
+  TP_RET_IF(split == TP_SPLIT_GATE_UP && !W_up, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w_shards, tp)) != TP_OK, st);
+  if (b) {
+    TP_RET_IF((st = check_ptr_array(reinterpret_cast<const void* const*>(b_shards), tp)) != TP_OK, st);
+    TP_RET_IF(!al_to(b, 4), TP_ERR_ALIGNMENT);
+    for (int i = 0; i < tp; ++i) TP_RET_IF(!al_to(b_shards[i], 4), TP_ERR_ALIGNMENT);
+  }
+  const int64_t es = esz(wdt);
+  TP_RET_IF(!al16(W) || (W_up && split == TP_SPLIT_GATE_UP && !al16(W_up)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((in_f * es) % 16 || (cols * es) % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(w_shards, tp)) != TP_OK, st);
+
+  ShardJob j;
+  j.split = split;
+  j.tp = tp;
+  j.esize = (int)es;
+  j.W = W;
+  j.W_up = (split == TP_SPLIT_GATE_UP) ? W_up : nullptr;
+  j.out_f = out_f;
+  j.in_f = in_f;
+  j.n_heads = n_heads;
+  j.n_kv_heads = n_kv_heads;
+  j.head_dim = head_dim;
+  j.rows = rows;
+  j.cols = cols;
+  j.b = b;
+  for (int i = 0; i < tp; ++i) {
+    j.dst[i] = w_shards[i];
+    j.b_dst[i] = b ? b_shards[i] : nullptr;
+  }
+  return launch_shard(j, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status column_parallel_linear(int tp, int64_t M, int64_t K, int64_t N, const void* X,
+                                 int64_t ldx, tp_dtype xdt, const void* const* w_shards,
+                                 const float* const* b_shards, tp_act act, void* Y, int64_t ldy,
+                                 tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || K <= 0 || N <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(N % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(xdt, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(!valid_act(act), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(act == TP_ACT_SWIGLU && b_shards, TP_ERR_UNSUPPORTED);
+  TP_RET_IF(ldx < K || ldy < N, TP_ERR_BAD_SHAPE);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(b_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  TP_RET_IF(!al16(X) || (ldx * es) % 16 || (K * es) % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(w_shards, tp)) != TP_OK, st);
+  LinearProblem p = column_problem(tp, M, K, N, X, ldx, xdt, w_shards, b_shards, act, Y, ldy,
+                                   ydt, N / tp);
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status row_parallel_linear(int tp, int64_t M, int64_t K, int64_t N, const void* X, int64_t ldx,
+                              tp_dtype xdt, const void* const* w_shards, const float* b, void* Y,
+                              int64_t ldy, tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || K <= 0 || N <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(K % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(xdt, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(ldx < K || ldy < N, TP_ERR_BAD_SHAPE);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  TP_RET_IF(!al16(X) || (ldx * es) % 16 || ((K / tp) * es) % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)) || (b && !al_to(b, 4)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(w_shards, tp)) != TP_OK, st);
+  LinearProblem p = row_problem(tp, M, K, N, X, ldx, xdt, w_shards, b, Y, ldy, ydt);
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_mlp_block(int tp, int64_t M, int64_t d_model, int64_t d_ff, tp_act act, tp_dtype xdt,
+                       const void* X, const void* const* w1_shards, const float* const* b1_shards,
+                       const void* const* w2_shards, const float* b2, void* h, void* Y,
+                       tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || d_model <= 0 || d_ff <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(d_ff % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(xdt, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(!valid_act(act), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(act == TP_ACT_SWIGLU && b1_shards, TP_ERR_UNSUPPORTED);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !h || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w1_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_ptr_array(w2_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(b1_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  TP_RET_IF(!al16(X) || !al16(h) || (d_model * es) % 16 || ((d_ff / tp) * es) % 16,
+            TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)) || (b2 && !al_to(b2, 4)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(w1_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_aligned_array(w2_shards, tp)) != TP_OK, st);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // h = act(X . W1_i^T + b1_i), shard i in columns [i*d_ff/tp, ...): stored in
+  // the input dtype (bf16 for bf16 inputs).
+  LinearProblem up = column_problem(tp, M, d_model, d_ff, X, d_model, xdt, w1_shards, b1_shards,
+                                    act, h, d_ff, xdt, d_ff / tp);
+  // Y = sum_i h_i . W2_i^T + b2
+  LinearProblem down = row_problem(tp, M, d_ff, d_model, h, d_ff, xdt, w2_shards, b2, Y, d_model,
+                                   ydt);
+  if ((st = run(up, s)) != TP_OK) return st;
+  return run(down, s);
+}
+
+tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads, int n_kv_heads,
+                       int head_dim, tp_dtype xdt, const void* X, const void* const* wqkv_shards,
+                       const float* const* bqkv_shards, void* qkv_out, tp_dtype qkv_dt,
+                       const void* ctx, const void* const* wo_shards, const float* bo, void* Y,
+                       tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || d_model <= 0 || n_heads < 1 || n_kv_heads < 1 || head_dim < 1,
+            TP_ERR_BAD_SHAPE);
+  TP_RET_IF(n_heads % tp || n_kv_heads % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(xdt, ydt) || !valid_io(xdt, qkv_dt), TP_ERR_DTYPE);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !qkv_out || !ctx || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(wqkv_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_ptr_array(wo_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(bqkv_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  const int64_t kq = (int64_t)n_heads * head_dim;        // ctx width
+  const int64_t ks = (int64_t)(n_heads / tp) * head_dim;  // ctx columns per shard
+  const int64_t ws = (int64_t)(n_heads / tp + 2 * (n_kv_heads / tp)) * head_dim;
+  TP_RET_IF(!al16(X) || !al16(ctx) || (d_model * es) % 16 || (kq * es) % 16 || (ks * es) % 16,
+            TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(qkv_out, esz(qkv_dt)) || !al_to(Y, esz(ydt)) || (bo && !al_to(bo, 4)),
+            TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(wqkv_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_aligned_array(wo_shards, tp)) != TP_OK, st);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // QKV: shard i -> qkv_out[i] = [M, ws]
+  LinearProblem qkv = column_problem(tp, M, d_model, ws * tp, X, d_model, xdt, wqkv_shards,
+                                     bqkv_shards, TP_ACT_NONE, qkv_out, ws, qkv_dt, M * ws);
+  // O: Y = sum_i ctx_i . Wo_i^T + bo
+  LinearProblem o = row_problem(tp, M, kq, d_model, ctx, kq, xdt, wo_shards, bo, Y, d_model, ydt);
+  if ((st = run(qkv, s)) != TP_OK) return st;
+  return run(o, s);
+}
+
+tp_status tp_device_status(tp_stream_t stream) {
+  return read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_selftest_bounded_wait(int64_t limit_ns, tp_stream_t stream) {
+  TP_RET_IF(limit_ns < 1 || limit_ns > 10000000000LL, TP_ERR_BAD_SHAPE);
+  return launch_bounded_wait_selftest(limit_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

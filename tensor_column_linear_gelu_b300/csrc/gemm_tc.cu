@@ -1,0 +1,531 @@
+// gemm_tc.cu -- tcgen05 / TMEM tensor-core GEMM fed by TMA, for bf16 calls
+// with many tokens (prefill-shaped).
+//
+//   column-parallel:  Y_i = act(X . W_i^T + b_i) for every shard i in one launch;
+//                     the shard index is a group of N-tiles, shard i's tiles
+//                     write its column block.  Fused epilogue: bias, erf-GELU,
+//                     or SwiGLU (the packed gate/up shard puts the 128 gate
+//                     columns and the matching 128 up columns of an output
+//                     group into one 256-wide tile).
+//   row-parallel:     Y = sum_i X_i . W_i^T + b.  The K loop walks shard 0's
+//                     k-blocks, then shard 1's, ... into ONE TMEM accumulator:
+//                     that accumulator is the all-reduce's sum.  The bias is
+//                     added once, in the epilogue.
+// ("Understanding Tensor Parallelism for Multi-GPU LLM Serving", "How Tensor
+// Parallelism Works Under the Hood"; "Tensor parallel serving",
+// "Column-parallel and row-parallel layers, paired".)
+//
+// Structure (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A (activations) and B (weights) k-blocks of
+//               64 bf16 (one 128-byte swizzle span) into a 4-stage ring.
+//   warp 1      TMEM allocation (512 columns: two 128x256 fp32 accumulators)
+//               and the single thread that issues tcgen05.mma (M=128, N=256,
+//               K=16, bf16 x bf16 -> fp32), committing each stage back to the
+//               producer and each finished tile to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               output row per thread), bias / activation in fp32, one
+//               rounding to the output dtype, stores.  Double buffering lets
+//               the epilogue of tile t overlap the mainloop of tile t+1.
+// Every mbarrier wait is bounded (sync.cuh); a wait that gives up records the
+// failure in the device error word, raises a CTA-wide abort flag, and every
+// role unwinds: in-flight TMA copies and MMAs are waited for (with a limit)
+// and TMEM is freed before the CTA exits.
+//
+// Summation order of an output element: k-blocks in increasing k (then, on
+// the row side, shard by shard), 4 MMAs of K=16 per k-block.  It does not
+// depend on N or tp, so column-parallel outputs are bit-identical to tp = 1.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sync.cuh"
+
+namespace tpla {
+namespace {
+
+constexpr int BM = 128;   // tokens per tile (TMEM lanes)
+constexpr int BN = 256;   // output columns per tile (MMA N)
+constexpr int BK = 64;    // k per stage: 64 bf16 = 128 bytes = one swizzle span
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_BUFS = 2;
+constexpr int TMEM_COLS = 512;        // ACC_BUFS x BN fp32 columns
+constexpr int THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+constexpr int64_t G = TP_GATE_UP_GROUP;
+static_assert(2 * G == BN, "a SwiGLU tile holds one gate/up group");
+static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
+
+struct alignas(64) GemmParams {
+  CUtensorMap tmA[TP_MAX_TP];  // column: [0] = X; row: X_i
+  CUtensorMap tmB[TP_MAX_TP];  // W_i
+  const float* bias[TP_MAX_TP];
+  void* Y;
+  unsigned int* err;
+  int64_t ldy, y_shard_stride;
+  int64_t M, ns, n_out;
+  int tp, row, act, ydt;
+  int m_tiles, n_tiles_per_shard, n_tiles, num_tiles;
+  int kb_per_shard, kb_total;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (SBO).  LBO is unused for this
+// layout (set to 1).  Bits 46-48 hold the fixed value 0b001.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- epilogue store
+// 32 consecutive outputs v[0..31] of one row at columns n0.. (n0 + 31), of
+// which the first `valid` exist.  Vector stores when the address allows.
+__device__ __forceinline__ void store_row32(void* Y, int ydt, int64_t base, int64_t n0, int valid,
+                                            const float (&v)[32]) {
+  if (ydt == TP_F32) {
+    float* p = reinterpret_cast<float*>(Y) + base + n0;
+    if (valid == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        reinterpret_cast<float4*>(p)[j] =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < valid) p[j] = v[j];
+    }
+  } else {
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(Y) + base + n0;
+    if (valid == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 q;
+        q.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+        q.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+        q.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+        q.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+        reinterpret_cast<uint4*>(p)[j] = q;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < valid) p[j] = __float2bfloat16_rn(v[j]);
+    }
+  }
+}
+
+__device__ __forceinline__ int valid_count(int64_t limit, int64_t n) {
+  const int64_t rem = limit - n;
+  return rem <= 0 ? 0 : (rem >= 32 ? 32 : (int)rem);
+}
+
+struct TileCoord {
+  int shard;   // column: shard of this tile; row: unused
+  int64_t m0;  // first token
+  int64_t n0;  // first row of W_i (column) or first output column (row)
+};
+
+// Tiles are numbered M-fastest: the CTAs running at the same time share the
+// weight tile(s) they stream and keep the activations in L2.
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
+  const int mt = tile % p.m_tiles;
+  const int nt = tile / p.m_tiles;
+  TileCoord c;
+  c.m0 = (int64_t)mt * BM;
+  if (p.row) {
+    c.shard = 0;
+    c.n0 = (int64_t)nt * BN;
+  } else {
+    c.shard = nt / p.n_tiles_per_shard;
+    c.n0 = (int64_t)(nt % p.n_tiles_per_shard) * BN;
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + ACC_BUFS;
+  uint64_t* drain = bars + 2 * STAGES + 2 * ACC_BUFS;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS) + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < ACC_BUFS; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    const int nmaps = p.row ? p.tp : 1;
+    for (int i = 0; i < nmaps; ++i) prefetch_tmap(&p.tmA[i]);
+    for (int i = 0; i < p.tp; ++i) prefetch_tmap(&p.tmB[i]);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t last_parity[STAGES];
+    bool issued[STAGES];
+    for (int s = 0; s < STAGES; ++s) issued[s] = false;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      const TileCoord c = tile_coord(p, tile);
+      for (int kb = 0; kb < p.kb_total; ++kb) {
+        const int sh = p.row ? kb / p.kb_per_shard : c.shard;
+        const int kk = p.row ? kb - sh * p.kb_per_shard : kb;
+        if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+          report_error(p.err, kErrTimeoutProducer);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[stage]);
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        tma_load_2d(smem_u32(sA + stage * A_BYTES), &p.tmA[p.row ? sh : 0], kk * BK, (int)c.m0, fb);
+        tma_load_2d(smem_u32(sB + stage * B_BYTES), &p.tmB[p.row ? sh : c.shard], kk * BK,
+                    (int)c.n0, fb);
+        issued[stage] = true;
+        last_parity[stage] = phase;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // wait (bounded) for every copy this thread started, so none lands after exit
+    for (int s = 0; s < STAGES; ++s)
+      if (issued[s] && !mbar_wait_bounded(smem_u32(&full[s]), last_parity[s], kWaitLimitNs))
+        report_error(p.err, kErrTimeoutDrain);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+        report_error(p.err, kErrTimeoutMma);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < p.kb_total; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs, abort_flag)) {
+          report_error(p.err, kErrTimeoutMma);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t adesc = sdesc_sw128(smem_u32(sA + stage * A_BYTES));
+        const uint64_t bdesc = sdesc_sw128(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+        for (int k = 0; k < BK / UMMA_K; ++k) {
+          // advance the start address by k * 32 bytes inside the swizzle span
+          mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), IDESC,
+                   (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&empty[stage]));  // stage reusable once these MMAs finish
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(smem_u32(&tfull[acc]));      // accumulator ready for the epilogue
+      if (++acc == ACC_BUFS) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // every MMA this thread issued has completed before TMEM is released
+    mma_commit(smem_u32(drain));
+    if (!mbar_wait_bounded(smem_u32(drain), 0, kWaitLimitNs)) report_error(p.err, kErrTimeoutDrain);
+  } else if (warp >= EPI_WARP0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;             // TMEM lane quadrant this warp may access
+    const int row_in_tile = q * 32 + lane;
+    const bool swiglu = (!p.row && p.act == TP_ACT_SWIGLU);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      // all lanes wait, then agree: tcgen05.ld below is warp-collective, so
+      // the warp must never split on a timeout
+      bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, kWaitLimitNs, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const TileCoord c = tile_coord(p, tile);
+      const int64_t m = c.m0 + row_in_tile;
+      const bool row_ok = m < p.M;
+      const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if (swiglu) {
+        // tile = one packed group: gate columns [0,128), up columns [128,256)
+        const int64_t out0 = (c.n0 / (2 * G)) * G;   // first output of the group (shard-local)
+        const int64_t base = (int64_t)c.shard * p.y_shard_stride + m * p.ldy;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          float g[32], u[32];
+          tmem_ld32(trow + ch * 32, g);
+          tmem_ld32(trow + G + ch * 32, u);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) g[j] = act_silu(g[j]) * u[j];
+          const int64_t n = out0 + ch * 32;
+          const int valid = valid_count(p.ns, n);
+          if (row_ok && valid > 0) store_row32(p.Y, p.ydt, base, n, valid, g);
+        }
+      } else {
+        const int64_t limit = p.row ? p.n_out : p.ns;
+        const int64_t base =
+            (p.row ? 0 : (int64_t)c.shard * p.y_shard_stride) + m * p.ldy;
+        const float* bias = p.row ? p.bias[0] : p.bias[c.shard];
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          float v[32];
+          tmem_ld32(trow + ch * 32, v);
+          const int64_t n = c.n0 + ch * 32;
+          const int valid = valid_count(limit, n);
+          if (bias) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < valid) v[j] += __ldg(bias + n + j);
+          }
+          if (!p.row && p.act == TP_ACT_GELU_ERF) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = act_gelu_erf(v[j]);
+          }
+          if (row_ok && valid > 0) store_row32(p.Y, p.ydt, base, n, valid, v);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (++acc == ACC_BUFS) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 K-major operand: `rows` rows of `inner` elements, row pitch
+// ld_bytes; boxes of 64 x box_rows with 128-byte swizzle; out-of-range
+// elements read as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld_bytes,
+              uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {ld_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Tokens above which the tensor-core GEMM takes a bf16 call (the GEMV handles
+// the rest).  Depends on M only.
+constexpr int64_t kGemvMaxTokens = 8;
+
+bool gemm_tc_supports(const LinearProblem& p) { return p.xdt == TP_BF16 && p.M > kGemvMaxTokens; }
+
+tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream) {
+  GemmParams gp{};
+  gp.err = device_error_word();
+  if (!gp.err) return TP_ERR_CUDA;
+  const int64_t es = 2;
+  if (p.row) {
+    for (int i = 0; i < p.tp; ++i) {
+      const void* xi = static_cast<const char*>(p.X) + (int64_t)i * p.x_shard_off * es;
+      if (!make_map(&gp.tmA[i], xi, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
+        return TP_ERR_CUDA;
+    }
+  } else {
+    if (!make_map(&gp.tmA[0], p.X, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
+      return TP_ERR_CUDA;
+  }
+  for (int i = 0; i < p.tp; ++i)
+    if (!make_map(&gp.tmB[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows, (uint64_t)(p.K * es), BN))
+      return TP_ERR_CUDA;
+  for (int i = 0; i < TP_MAX_TP; ++i) gp.bias[i] = p.bias[i];
+  gp.Y = p.Y;
+  gp.ldy = p.ldy;
+  gp.y_shard_stride = p.y_shard_stride;
+  gp.M = p.M;
+  gp.ns = p.ns;
+  gp.n_out = p.n_out;
+  gp.tp = p.tp;
+  gp.row = p.row ? 1 : 0;
+  gp.act = p.act;
+  gp.ydt = p.ydt;
+  gp.m_tiles = (int)((p.M + BM - 1) / BM);
+  gp.kb_per_shard = (int)((p.K + BK - 1) / BK);
+  if (p.row) {
+    gp.n_tiles_per_shard = (int)((p.n_out + BN - 1) / BN);
+    gp.n_tiles = gp.n_tiles_per_shard;
+    gp.kb_total = gp.kb_per_shard * p.tp;
+  } else {
+    gp.n_tiles_per_shard = (int)((p.w_rows + BN - 1) / BN);
+    gp.n_tiles = gp.n_tiles_per_shard * p.tp;
+    gp.kb_total = gp.kb_per_shard;
+  }
+  const int64_t tiles = (int64_t)gp.m_tiles * gp.n_tiles;
+  if (tiles > INT32_MAX) return TP_ERR_BAD_SHAPE;
+  gp.num_tiles = (int)tiles;
+
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return TP_ERR_CUDA;
+  const int grid = (int)std::min<int64_t>(tiles, sm_count());
+  gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(gp);
+  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // namespace tpla

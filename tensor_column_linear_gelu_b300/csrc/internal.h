@@ -1,0 +1,74 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units.  Not part of the public interface (that is include/tpla.h).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "tpla.h"
+
+namespace tpla {
+
+// One linear problem of the tensor-parallel path, after validation.
+//
+// Column-parallel (row == false): output o in [0, n_out) belongs to shard
+//   i = o / ns at local column n = o % ns; it is act(X[m,:] . W_i[n,:] + b_i[n])
+//   stored at Y + i*y_shard_stride + m*ldy + n.  For SwiGLU, W_i is the packed
+//   gate/up shard (groups of TP_GATE_UP_GROUP gate rows, then as many up rows).
+// Row-parallel (row == true): output o in [0, n_out) is
+//   sum_i X_i[m,:] . W_i[o,:] + bias[0][o], with X_i = X + i*x_shard_off and
+//   W_i of shape [n_out, K]; K is the per-shard input width.
+struct LinearProblem {
+  int tp = 1;
+  bool row = false;
+  int act = TP_ACT_NONE;
+  int xdt = TP_BF16;
+  int ydt = TP_BF16;
+  int64_t M = 0;
+  int64_t K = 0;            // input features per shard (column: all of K)
+  int64_t n_out = 0;        // outputs over all shards (column) or N (row)
+  int64_t ns = 0;           // outputs per shard (column); n_out (row)
+  int64_t w_rows = 0;       // rows of each weight shard buffer
+  const void* X = nullptr;
+  int64_t ldx = 0;
+  int64_t x_shard_off = 0;  // row: element offset of X_i
+  const void* W[TP_MAX_TP] = {};
+  const float* bias[TP_MAX_TP] = {};
+  void* Y = nullptr;
+  int64_t ldy = 0;
+  int64_t y_shard_stride = 0;  // column: element offset of shard i's output
+};
+
+// Weight-streaming GEMV on CUDA cores (few tokens; also the fp32 path).
+tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream);
+
+// tcgen05 / TMEM tensor-core GEMM fed by TMA (bf16; many tokens).
+tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream);
+bool gemm_tc_supports(const LinearProblem& p);
+
+// Shard / pack copies.
+struct ShardJob {
+  int split = 0;
+  int tp = 1;
+  int esize = 2;
+  const void* W = nullptr;
+  const void* W_up = nullptr;
+  int64_t out_f = 0, in_f = 0;
+  int n_heads = 0, n_kv_heads = 0, head_dim = 0;
+  int64_t rows = 0, cols = 0;   // shape of one shard
+  void* dst[TP_MAX_TP] = {};
+  const float* b = nullptr;
+  float* b_dst[TP_MAX_TP] = {};
+};
+tp_status launch_shard(const ShardJob& j, cudaStream_t stream);
+
+// Device-side error word (bounded waits) and its self-test.
+unsigned int* device_error_word();
+tp_status read_and_clear_device_error(cudaStream_t stream);
+tp_status launch_bounded_wait_selftest(int64_t limit_ns, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace tpla
