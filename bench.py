@@ -113,16 +113,64 @@ def traffic_record(workload):
 
 
 # ------------------------------------------------------------------ clocks
+class _Nvml:
+    """Read-only NVML queries: the pynvml module when installed, else the same C
+    functions of the driver's libnvidia-ml.so.1 through ctypes."""
+
+    CLOCK_SM = 1
+    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+                   ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, uuid: str):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._p, self._h = pynvml, pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.kind = "pynvml"
+            return
+        except ImportError:
+            pass
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByUUID failed")
+        self._p, self._lib, self._h, self._ct = None, lib, h, ctypes
+        self.kind = "libnvidia-ml (ctypes)"
+
+    def _u32(self, fn, *args):
+        v = self._ct.c_uint()
+        if fn(self._h, *args, self._ct.byref(v)) != 0:
+            raise RuntimeError("nvml query failed")
+        return v.value
+
+    def sm_clock(self):
+        if self._p:
+            return self._p.nvmlDeviceGetClockInfo(self._h, self.CLOCK_SM)
+        return self._u32(self._lib.nvmlDeviceGetClockInfo, self.CLOCK_SM)
+
+    def max_sm_clock(self):
+        if self._p:
+            return self._p.nvmlDeviceGetMaxClockInfo(self._h, self.CLOCK_SM)
+        return self._u32(self._lib.nvmlDeviceGetMaxClockInfo, self.CLOCK_SM)
+
+    def reasons(self):
+        if self._p:
+            r = self._p.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+        else:
+            v = self._ct.c_ulonglong()
+            if self._lib.nvmlDeviceGetCurrentClocksEventReasons(self._h, self._ct.byref(v)) != 0:
+                raise RuntimeError("nvml query failed")
+            r = v.value
+        return {n for n, bit in self.REASON_BITS if r & bit}
+
+
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons of one GPU, polled through NVML
     every `period_s` on a background thread while the timed region runs (reading
     only: no setting is changed).  Works for timed regions of a few milliseconds."""
-
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
-               ("hw_power_brake_slowdown", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
     def __init__(self, device_index: int, period_s: float = 0.002):
         self.device_index = device_index
@@ -131,38 +179,30 @@ class ClockSampler:
         self.reasons = set()
         self.max_mhz = None
         self.error = None
+        self.kind = None
         self._stop = None
         self._thread = None
 
-    def _handle(self):
-        import pynvml
-        import torch
-        uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
-        if not uuid.startswith("GPU-"):
-            uuid = "GPU-" + uuid
-        return pynvml.nvmlDeviceGetHandleByUUID(uuid)
-
     def __enter__(self):
         import threading
+        import torch
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            h = self._handle()
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            nv = _Nvml(uuid)
+            self.kind = nv.kind
+            self.max_mhz = nv.max_sm_clock()
         except Exception as e:  # noqa: BLE001 - report, do not fail the benchmark
-            self.error = f"nvml unavailable: {type(e).__name__}"
+            self.error = f"nvml unavailable: {type(e).__name__}: {e}"
             return self
         self._stop = threading.Event()
 
         def poll():
-            masks = [(n, getattr(pynvml, a)) for n, a in self.REASONS]
             while True:
                 try:
-                    self.samples.append(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
-                    r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-                    for n, m in masks:
-                        if r & m:
-                            self.reasons.add(n)
+                    self.samples.append(nv.sm_clock())
+                    self.reasons |= nv.reasons()
                 except Exception as e:  # noqa: BLE001
                     self.error = f"nvml query failed: {type(e).__name__}"
                     return
@@ -184,7 +224,7 @@ class ClockSampler:
                     "reasons": [self.error or "no samples"]}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples),
-                "source": "nvml, polled every %g ms" % (self.period_s * 1e3)}
+                "source": f"{self.kind}, polled every {self.period_s * 1e3:g} ms"}
 
 
 # ------------------------------------------------------------------ ranks
