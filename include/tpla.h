@@ -278,6 +278,47 @@ tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads,
                        tp_dtype ydt, tp_stream_t stream);
 
 /*
+ * Size in bytes of the workspace built into the library for
+ * tp_mlp_block_noalloc (8 MiB).
+ */
+#define TP_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * tp_mlp_block_noalloc -- tp_mlp_block without a caller-provided workspace.
+ *
+ * No passage of the pages has a counterpart to this call; it exists for users
+ * of this library.  tp_mlp_block needs a [M, d_ff] device workspace for the
+ * intermediate activation h.  Some callers cannot allocate one: their device
+ * memory belongs to another allocator (a serving engine that reserves the
+ * GPU at start-up, a plugin whose host application hands out no device
+ * memory), or cudaMalloc is off limits on their path because it can
+ * synchronise the device and stall unrelated work.  This call keeps h in a
+ * fixed buffer of TP_NOALLOC_SCRATCH_BYTES that is part of the library image:
+ * every GPU that loads the library holds it until the process exits.  The call
+ * itself allocates nothing (no cudaMalloc, no cudaFree).
+ *
+ *   Limit       M * d_ff * (2 for TP_BF16, 4 for TP_F32) <= TP_NOALLOC_SCRATCH_BYTES,
+ *               e.g. up to 146 tokens at d_ff = 28672 in bf16.  Larger calls
+ *               return TP_ERR_UNSUPPORTED and launch nothing.
+ *   Set-up      the first call on a device looks up the buffer's device
+ *               address (with that device current).  Make that first call
+ *               before any stream capture on the device.
+ *   Sharing     every call on a device uses the same buffer, which keeps the
+ *               last call's contents.  Nothing in it needs to start at zero:
+ *               each call writes all of its h before reading it.  Calls that
+ *               can run at the same time on the GPU (different streams with no
+ *               ordering between them) race on the buffer and give wrong
+ *               results: order them.
+ *   Arguments, results and other errors: as tp_mlp_block, without h.
+ */
+tp_status tp_mlp_block_noalloc(int tp, int64_t M, int64_t d_model, int64_t d_ff,
+                               tp_act act, tp_dtype xdt, const void* X,
+                               const void* const* w1_shards,
+                               const float* const* b1_shards,
+                               const void* const* w2_shards, const float* b2,
+                               void* Y, tp_dtype ydt, tp_stream_t stream);
+
+/*
  * tp_device_status -- synchronise `stream`, then report and clear the
  * library's device-side error word on the current device.  Every spin-wait
  * inside the library's kernels is bounded; a wait that runs out sets this

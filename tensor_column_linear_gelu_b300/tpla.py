@@ -33,6 +33,7 @@ TP_ACT_NONE, TP_ACT_GELU_ERF, TP_ACT_SWIGLU = 0, 1, 2
 TP_SPLIT_COLUMN, TP_SPLIT_ROW, TP_SPLIT_QKV_HEADS, TP_SPLIT_GATE_UP = 0, 1, 2, 3
 TP_MAX_TP = 16
 TP_GATE_UP_GROUP = 128
+TP_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 ACTS = {"none": TP_ACT_NONE, "gelu": TP_ACT_GELU_ERF, "swiglu": TP_ACT_SWIGLU}
 SPLITS = {"column": TP_SPLIT_COLUMN, "row": TP_SPLIT_ROW, "qkv_heads": TP_SPLIT_QKV_HEADS,
@@ -42,7 +43,7 @@ _DT = {torch.float32: TP_F32, torch.bfloat16: TP_BF16}
 # Every symbol include/tpla.h declares.
 EXPORTS = ("tp_status_string", "tp_shard_shape", "tp_shard_weights", "column_parallel_linear",
            "row_parallel_linear", "tp_mlp_block", "tp_attn_proj", "tp_device_status",
-           "tp_selftest_bounded_wait")
+           "tp_selftest_bounded_wait", "tp_mlp_block_noalloc")
 
 # ----------------------------------------------------------------- prototypes
 _vp = ctypes.c_void_p
@@ -64,6 +65,8 @@ lib.tp_mlp_block.argtypes = [_int, _i64, _i64, _i64, _int, _int, _vp, _vpp, _vpp
                              _vp, _int, _vp]
 lib.tp_attn_proj.argtypes = [_int, _i64, _i64, _int, _int, _int, _int, _vp, _vpp, _vpp, _vp, _int,
                              _vp, _vpp, _vp, _vp, _int, _vp]
+lib.tp_mlp_block_noalloc.argtypes = [_int, _i64, _i64, _i64, _int, _int, _vp, _vpp, _vpp, _vpp,
+                                     _vp, _vp, _int, _vp]
 lib.tp_device_status.argtypes = [_vp]
 lib.tp_selftest_bounded_wait.argtypes = [_i64, _vp]
 for _name in EXPORTS[1:]:
@@ -215,6 +218,26 @@ def tp_attn_proj(tp: int, X: torch.Tensor, wqkv_shards, bqkv_shards, ctx: torch.
                             ptr(Y), dtype_code(Y.dtype), stream_handle(stream)),
            "tp_attn_proj")
     return qkv_out, Y
+
+
+def tp_mlp_block_noalloc(tp: int, X: torch.Tensor, w1_shards, b1_shards, w2_shards,
+                         b2: Optional[torch.Tensor], act="gelu", d_ff: Optional[int] = None,
+                         out_dtype: Optional[torch.dtype] = None, Y: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """The FFN block with h kept in the library's built-in workspace, for callers
+    that cannot allocate device memory (M * d_ff * element size must fit
+    TP_NOALLOC_SCRATCH_BYTES).  Returns Y; Y must be preallocated by such callers."""
+    M, d_model = X.shape
+    if d_ff is None:
+        d_ff = w2_shards[0].shape[1] * tp
+    if Y is None:
+        Y = torch.empty(M, d_model, dtype=out_dtype or X.dtype, device=X.device)
+    _check(lib.tp_mlp_block_noalloc(tp, M, d_model, d_ff, _act(act), dtype_code(X.dtype), ptr(X),
+                                    ptr_array(w1_shards), ptr_array(b1_shards),
+                                    ptr_array(w2_shards), ptr(b2), ptr(Y), dtype_code(Y.dtype),
+                                    stream_handle(stream)),
+           "tp_mlp_block_noalloc")
+    return Y
 
 
 def tp_device_status(stream=None) -> int:
