@@ -68,10 +68,17 @@ tp_status check_bias_array(const float* const* b, int tp) {
   return TP_OK;
 }
 
-// The one place a validated problem picks its kernel.
+// The one place a validated problem picks its kernel.  The choice depends on
+// the dtype and the token count M only (never on N or tp):
+//   fp32, or bf16 with M <= kGemvMaxTokens      weight-streaming GEMV (CUDA cores)
+//   bf16, kGemvMaxTokens < M <= kSkinnyMaxTokens  tcgen05 decode kernel
+//   bf16, M > kSkinnyMaxTokens                    tcgen05 prefill GEMM
 tp_status run(const LinearProblem& p, cudaStream_t s) {
   if (p.M == 0) return TP_OK;
-  if (p.xdt == TP_BF16 && gemm_tc_supports(p)) return launch_gemm_tc(p, s);
+  if (p.xdt == TP_BF16 && p.M > kGemvMaxTokens) {
+    if (p.M <= kSkinnyMaxTokens) return launch_skinny(p, s);
+    return launch_gemm_tc(p, s);
+  }
   return launch_gemv(p, s);
 }
 

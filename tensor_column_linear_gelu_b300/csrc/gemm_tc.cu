@@ -43,6 +43,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "sync.cuh"
+#include "tc_ptx.cuh"
 
 namespace tpla {
 namespace {
@@ -77,120 +78,6 @@ struct alignas(64) GemmParams {
   int m_tiles, n_tiles_per_shard, n_tiles, num_tiles;
   int kb_per_shard, kb_total;
 };
-
-// ---------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row groups 1024 bytes apart (SBO).  LBO is unused for this
-// layout (set to 1).  Bits 46-48 hold the fixed value 0b001.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;
-  d |= (uint64_t)(1024 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t idesc_bf16_f32(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every tcgen05 operation issued so far by this thread
-// has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// ---------------------------------------------------------------- epilogue store
-// 32 consecutive outputs v[0..31] of one row at columns n0.. (n0 + 31), of
-// which the first `valid` exist.  Vector stores when the address allows.
-__device__ __forceinline__ void store_row32(void* Y, int ydt, int64_t base, int64_t n0, int valid,
-                                            const float (&v)[32]) {
-  if (ydt == TP_F32) {
-    float* p = reinterpret_cast<float*>(Y) + base + n0;
-    if (valid == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        reinterpret_cast<float4*>(p)[j] =
-            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < valid) p[j] = v[j];
-    }
-  } else {
-    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(Y) + base + n0;
-    if (valid == 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 q;
-        q.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-        q.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-        q.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-        q.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-        reinterpret_cast<uint4*>(p)[j] = q;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < valid) p[j] = __float2bfloat16_rn(v[j]);
-    }
-  }
-}
 
 __device__ __forceinline__ int valid_count(int64_t limit, int64_t n) {
   const int64_t rem = limit - n;
@@ -258,11 +145,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     for (int i = 0; i < p.tp; ++i) prefetch_tmap(&p.tmB[i]);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(const_cast<uint32_t*>(tmem_slot))),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
   }
   tc_fence_before();
   __syncthreads();
@@ -427,13 +310,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
+    tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------- host side
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -447,12 +331,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   });
   return fn;
 }
+}  // namespace
 
-// 2-D bf16 K-major operand: `rows` rows of `inner` elements, row pitch
-// ld_bytes; boxes of 64 x box_rows with 128-byte swizzle; out-of-range
-// elements read as zero.
-bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t ld_bytes,
-              uint32_t box_rows) {
+bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t ld_bytes, uint32_t box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, rows};
@@ -464,14 +346,6 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-// Tokens above which the tensor-core GEMM takes a bf16 call (the GEMV handles
-// the rest).  Depends on M only.
-constexpr int64_t kGemvMaxTokens = 8;
-
-bool gemm_tc_supports(const LinearProblem& p) { return p.xdt == TP_BF16 && p.M > kGemvMaxTokens; }
-
 tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream) {
   GemmParams gp{};
   gp.err = device_error_word();
@@ -480,15 +354,15 @@ tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream) {
   if (p.row) {
     for (int i = 0; i < p.tp; ++i) {
       const void* xi = static_cast<const char*>(p.X) + (int64_t)i * p.x_shard_off * es;
-      if (!make_map(&gp.tmA[i], xi, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
+      if (!make_tma_map_bf16(&gp.tmA[i], xi, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
         return TP_ERR_CUDA;
     }
   } else {
-    if (!make_map(&gp.tmA[0], p.X, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
+    if (!make_tma_map_bf16(&gp.tmA[0], p.X, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
       return TP_ERR_CUDA;
   }
   for (int i = 0; i < p.tp; ++i)
-    if (!make_map(&gp.tmB[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows, (uint64_t)(p.K * es), BN))
+    if (!make_tma_map_bf16(&gp.tmB[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows, (uint64_t)(p.K * es), BN))
       return TP_ERR_CUDA;
   for (int i = 0; i < TP_MAX_TP; ++i) gp.bias[i] = p.bias[i];
   gp.Y = p.Y;

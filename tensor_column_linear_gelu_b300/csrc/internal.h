@@ -4,6 +4,7 @@
 
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "tpla.h"
@@ -45,7 +46,19 @@ tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream);
 
 // tcgen05 / TMEM tensor-core GEMM fed by TMA (bf16; many tokens).
 tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream);
-bool gemm_tc_supports(const LinearProblem& p);
+
+// tcgen05 decode kernel with the weights as the MMA's M operand (bf16; a
+// handful of tokens, up to kSkinnyMaxTokens).
+constexpr int64_t kSkinnyMaxTokens = 128;
+// bf16 calls with at most this many tokens go to the GEMV.
+constexpr int64_t kGemvMaxTokens = 4;
+tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream);
+
+// 2-D bf16 tensor map for TMA: `rows` rows of `inner` elements, row pitch
+// ld_bytes, boxes of 64 elements (one 128-byte swizzle span) x box_rows rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t ld_bytes, uint32_t box_rows);
 
 // Shard / pack copies.
 struct ShardJob {

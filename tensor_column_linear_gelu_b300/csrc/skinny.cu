@@ -1,0 +1,600 @@
+// skinny.cu -- tcgen05 / TMEM kernel for decode-shaped bf16 calls: a handful
+// of tokens (up to kSkinnyMaxTokens) against a large weight.
+//
+// With few tokens a linear layer reads every weight byte once and does about
+// M FLOPs per byte, so it is bound by HBM bandwidth: each device streams its
+// own slice of the weights ("What is tensor parallelism?", "Why it helps when
+// serving").  Three measured facts shape the kernel:
+//   * a tcgen05.mma of M=128, K=16 occupies the tensor core for about the same
+//     time whatever N is, so the weights must be the N operand: one MMA then
+//     consumes up to 256 weight rows x 16 k (8 KB).  The tokens are the
+//     128-row A operand; only the first M rows are loaded, the other rows of
+//     the A tile (whatever shared memory holds) only produce TMEM lanes that
+//     nothing reads;
+//   * TMA streaming reaches the HBM roofline with 128-byte-wide boxes, so a
+//     deep ring of (X box, weight rows) stages per SM is enough;
+//   * every SM must stream about the same number of bytes, or the SMs that
+//     finish early leave bandwidth unused.
+//
+//   column-parallel:  Y_i = act(X . W_i^T + b_i).  CTA b of a persistent grid
+//                     owns the output features [b*F/grid, (b+1)*F/grid) in
+//                     units of 8 (features numbered shard-major).  The range
+//                     is cut into pieces that stay inside one shard (and, for
+//                     SwiGLU, one gate/up group), and consecutive pieces are
+//                     packed at 8-row slots into B tiles of 256 weight rows,
+//                     so a CTA runs as few K loops as its bytes allow.  Every
+//                     output accumulates over all of K in one TMEM column --
+//                     no split-K -- so its summation order depends on K only
+//                     and sharded results are bit-identical to tp = 1.
+//                     SwiGLU: a piece's gate rows sit at its slot among the
+//                     tile's first R rows and its up rows at the same slot
+//                     among the next R (R = slot rows of the tile, <= 128);
+//                     the MMA runs N = 2R and the thread that owns a token
+//                     reads gate column slot+j and up column R+slot+j.
+//   row-parallel:     Y = sum_i X_i . W_i^T + b.  The outputs are cut into
+//                     tiles of 256; each tile belongs to a thread-block
+//                     cluster of cs CTAs that split the K loop (shard 0's
+//                     k-blocks, then shard 1's, ...) into cs contiguous parts.
+//                     Each CTA's partial sum goes TMEM -> its shared memory;
+//                     after a cluster barrier CTA r adds the cs partials of
+//                     its slice of the tile in rank order (distributed shared
+//                     memory loads), adds the bias once and stores.  With
+//                     cs = tp each CTA holds exactly one shard's partial and
+//                     the cluster reduction is the all-reduce's sum.
+// ("Understanding Tensor Parallelism for Multi-GPU LLM Serving", "How Tensor
+// Parallelism Works Under the Hood"; "Tensor parallel serving",
+// "Column-parallel and row-parallel layers, paired".)
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: per k-block one X box {64, xrows} (lane 0) and
+//               the tile's weight rows as 64-row and 16-row boxes, one box
+//               per lane: a single thread issuing many small boxes cannot
+//               keep the TMA unit busy.
+//   warp 1      TMEM allocation (512 columns: two 128 x 256 fp32 accumulators)
+//               and the single thread issuing tcgen05.mma (M=128, N<=256,
+//               K=16), committing each stage back to the producer and each
+//               finished chunk to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld (one TMEM lane = one token per thread),
+//               bias / activation in fp32, one rounding, row stores; on the
+//               row side the partial goes to shared memory for the cluster
+//               reduction.
+// Every mbarrier wait is bounded (sync.cuh); a wait that gives up records the
+// failure in the device error word and that role stops issuing work.  Every
+// thread of every CTA still reaches both cluster barriers, so a failure can
+// never leave a peer CTA waiting.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sync.cuh"
+#include "tc_ptx.cuh"
+
+namespace tpla {
+namespace {
+
+constexpr int SK_THREADS = 192;
+constexpr int SK_EPI_WARP0 = 2;
+constexpr int SK_BK = 64;                   // k per stage: one 128-byte swizzle span
+constexpr int SK_UMMA_K = 16;
+constexpr int SK_ROW_BYTES = SK_BK * 2;     // 128 bytes per staged row
+constexpr int SK_A_BYTES = 128 * SK_ROW_BYTES;  // the A tile one MMA reads (128 rows)
+constexpr int SK_BN = 256;                  // weight rows per B tile (MMA N)
+constexpr int SK_B_BYTES = SK_BN * SK_ROW_BYTES;  // 32 KB
+constexpr int SK_MAX_STAGES = 16;
+constexpr int SK_ACC_BUFS = 2;
+constexpr int SK_TMEM_COLS = SK_ACC_BUFS * SK_BN;
+constexpr int SK_GRAIN = 16;                // features per balance unit (column side)
+constexpr int SK_MAX_BOXES = 31;            // weight boxes per stage (one per producer lane)
+constexpr int SK_MAX_CLUSTER = 8;
+constexpr int SK_RED_PITCH = SK_BN + 4;     // floats per token row of a reduction buffer
+constexpr int SK_NUM_BARS = 2 * SK_MAX_STAGES + 2 * SK_ACC_BUFS + 1;
+constexpr int SK_BAR_BYTES = SK_NUM_BARS * 8 + 16;
+constexpr int SK_SMEM_MAX = 232448;         // dynamic shared memory per CTA (227 KB)
+constexpr int64_t G = TP_GATE_UP_GROUP;
+static_assert(2 * G == SK_BN, "a SwiGLU chunk's gate and up rows fill one B tile");
+
+struct SkinnyParams {
+  CUtensorMap tmX[TP_MAX_TP];    // column: [0] = X; row: X_i.  Box {64, xrows}.
+  CUtensorMap tmW16[TP_MAX_TP];  // W_i, box {64, 16}
+  CUtensorMap tmW64[TP_MAX_TP];  // W_i, box {64, 64}
+  const float* bias[TP_MAX_TP];
+  void* Y;
+  unsigned int* err;
+  int64_t ldy, y_shard_stride;
+  int64_t M, ns, feat_total;     // feat_total: column tp*ns; row n_out
+  int tp, row, act, ydt;
+  int xrows, x_stage_bytes, stages;
+  int kb_per_shard, kb_total;
+  int cs;                        // row side: CTAs per cluster splitting K
+};
+
+__device__ __forceinline__ int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
+
+constexpr int SK_MAX_PIECES = 8;
+
+// One B tile's worth of work: up to SK_MAX_PIECES pieces of consecutive
+// output features, each at a 16-row slot of the tile, and the k-blocks of its
+// K loop.
+struct Piece {
+  int shard;    // column: shard of the piece; row: unused (per k-block)
+  int64_t loc;  // column: first shard-local feature; row: first output
+  int c;        // features (outputs) in the piece
+  int slot;     // first row of the piece in the B tile (a multiple of 16)
+};
+struct Tile {
+  int n;        // pieces
+  int rows;     // slot rows used (a multiple of 16)
+  int boxes;    // weight TMA boxes per stage
+  int kb0, kb1; // k-blocks [kb0, kb1) of the tile's K loop
+  Piece pc[SK_MAX_PIECES];
+};
+
+// Weight boxes of a piece of c rows: whole 64-row boxes, then 16-row boxes.
+__device__ __forceinline__ int piece_boxes(int c) { return c / 64 + ((c % 64) + 15) / 16; }
+
+// Box `want` (0-based) of a tile, in the order pieces, then gate/up halves,
+// then rows: which piece and half, its first row within the piece, and its
+// height.  Returns false when the tile has fewer boxes.
+__device__ __forceinline__ bool tile_box(const Tile& t, bool swiglu, int want, int& piece,
+                                         int& half, int& r, int& h) {
+  int b = 0;
+  for (int i = 0; i < t.n; ++i)
+    for (int hf = 0; hf < (swiglu ? 2 : 1); ++hf) {
+      const int c = t.pc[i].c;
+      for (int rr = 0; rr < c; ++b) {
+        const int hh = (rr + 64 <= c) ? 64 : 16;
+        if (b == want) {
+          piece = i;
+          half = hf;
+          r = rr;
+          h = hh;
+          return true;
+        }
+        rr += hh;
+      }
+    }
+  return false;
+}
+
+// Column side: the tile starting at global feature f of a range ending at f1;
+// advances f past the features it takes.
+__device__ __forceinline__ Tile column_tile(const SkinnyParams& p, int64_t& f, int64_t f1) {
+  const bool swiglu = p.act == TP_ACT_SWIGLU;
+  const int cap = swiglu ? (int)G : SK_BN;  // slot rows per tile (features for SwiGLU)
+  Tile t;
+  t.n = 0;
+  t.rows = 0;
+  t.kb0 = 0;
+  t.kb1 = p.kb_total;
+  t.boxes = 0;
+  while (f < f1 && t.n < SK_MAX_PIECES && t.rows < cap) {
+    const int64_t sh = f / p.ns;
+    const int64_t loc = f - sh * p.ns;
+    int64_t lim = imin(f1 - f, p.ns - loc);
+    if (swiglu) lim = imin(lim, G - loc % G);
+    const int c = (int)imin(lim, cap - t.rows);
+    const int nb = piece_boxes(c) * (swiglu ? 2 : 1);
+    if (t.n > 0 && t.boxes + nb > SK_MAX_BOXES) break;
+    t.pc[t.n].shard = (int)sh;
+    t.pc[t.n].loc = loc;
+    t.pc[t.n].c = c;
+    t.pc[t.n].slot = t.rows;
+    ++t.n;
+    t.boxes += nb;
+    t.rows += (c + 15) / 16 * 16;
+    f += c;
+  }
+  return t;
+}
+
+// Column side: this CTA's feature range [f0, f1), balanced in units of 8.
+__device__ __forceinline__ void column_range(const SkinnyParams& p, int64_t& f0, int64_t& f1) {
+  const int64_t units = (p.feat_total + SK_GRAIN - 1) / SK_GRAIN;
+  const int64_t u0 = (int64_t)blockIdx.x * units / gridDim.x;
+  const int64_t u1 = ((int64_t)blockIdx.x + 1) * units / gridDim.x;
+  f0 = imin(u0 * SK_GRAIN, p.feat_total);
+  f1 = imin(u1 * SK_GRAIN, p.feat_total);
+}
+
+// Row side: the one tile of this CTA -- its cluster's 256 outputs and its
+// rank's share of the k-blocks.
+__device__ __forceinline__ Tile row_tile(const SkinnyParams& p, int rank) {
+  Tile t;
+  const int64_t tile = blockIdx.x / p.cs;
+  t.n = 1;
+  t.pc[0].shard = 0;
+  t.pc[0].loc = tile * SK_BN;
+  t.pc[0].c = (int)imin(SK_BN, p.feat_total - t.pc[0].loc);
+  t.pc[0].slot = 0;
+  t.rows = (t.pc[0].c + 15) / 16 * 16;
+  t.boxes = piece_boxes(t.pc[0].c);
+  t.kb0 = (int)((int64_t)rank * p.kb_total / p.cs);
+  t.kb1 = (int)((int64_t)(rank + 1) * p.kb_total / p.cs);
+  return t;
+}
+
+// Loop over this CTA's tiles: the column side walks its feature range, the
+// row side has one tile.
+#define SK_FOR_EACH_TILE(tl, ...)                                     \
+  do {                                                                \
+    if (p.row) {                                                      \
+      const Tile tl = row_tile(p, rank);                              \
+      __VA_ARGS__                                                     \
+    } else {                                                          \
+      for (int64_t f_ = f0; f_ < f1;) {                               \
+        const Tile tl = column_tile(p, f_, f1);                       \
+        __VA_ARGS__                                                   \
+      }                                                               \
+    }                                                                 \
+  } while (0)
+
+__global__ void __launch_bounds__(SK_THREADS, 1)
+    skinny_kernel(const __grid_constant__ SkinnyParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  uint8_t* sX = smem;                                      // S x-stages, then
+  uint8_t* sW = smem + (size_t)S * p.x_stage_bytes;        // S weight stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sW + (size_t)S * SK_B_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + SK_MAX_STAGES;
+  uint64_t* tfull = bars + 2 * SK_MAX_STAGES;
+  uint64_t* tempty = tfull + SK_ACC_BUFS;
+  uint64_t* drain = tempty + SK_ACC_BUFS;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + SK_NUM_BARS);
+  // Row side: after the K loop the ring is reused as this CTA's reduction
+  // buffer red[token][SK_RED_PITCH] (fp32).
+  float* red = reinterpret_cast<float*>(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool swiglu = (!p.row && p.act == TP_ACT_SWIGLU);
+  const int rank = p.row ? (int)cluster_ctarank() : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < SK_ACC_BUFS; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(smem_u32(drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    const int nx = p.row ? p.tp : 1;
+    for (int i = 0; i < nx; ++i) prefetch_tmap(&p.tmX[i]);
+    for (int i = 0; i < p.tp; ++i) {
+      prefetch_tmap(&p.tmW16[i]);
+      prefetch_tmap(&p.tmW64[i]);
+    }
+  }
+  if (warp == 1) tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), SK_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int64_t f0 = 0, f1 = 0;
+  if (!p.row) column_range(p, f0, f1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // The whole warp issues: lane 0 waits for the stage, arms its barrier and
+    // loads the X box; lane 1 + b loads weight box b of the tile.  Issuing the
+    // boxes from many lanes keeps the TMA unit fed.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    SK_FOR_EACH_TILE(tl, {
+      if (ok) {
+        int piece = 0, half = 0, r = 0, h = 0;
+        const bool mine = lane > 0 && tile_box(tl, swiglu, lane - 1, piece, half, r, h);
+        int64_t wrow = 0;     // first weight row of this lane's box in its shard buffer
+        uint32_t woff = 0;    // its offset in the stage's B tile
+        int wshard = 0;
+        if (mine) {
+          const Piece& pc = tl.pc[piece];
+          wrow = (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G + half * G : pc.loc) + r;
+          woff = (uint32_t)(pc.slot + half * tl.rows + r) * SK_ROW_BYTES;
+          wshard = pc.shard;
+        }
+        uint32_t bytes = 0;
+        if (lane == 0) {
+          bytes = (uint32_t)p.x_stage_bytes;
+          for (int b = 0; b < tl.boxes; ++b) {
+            int pi, hf, rr, hh;
+            if (tile_box(tl, swiglu, b, pi, hf, rr, hh)) bytes += (uint32_t)hh * SK_ROW_BYTES;
+          }
+        }
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+          const int rsh = p.row ? kb / p.kb_per_shard : 0;  // row side: shard of this k-block
+          const int kk = p.row ? kb - rsh * p.kb_per_shard : kb;
+          bool got = true;
+          if (lane == 0) got = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            if (lane == 0) report_error(p.err, kErrTimeoutProducer);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, bytes);
+            tma_load_2d(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh], kk * SK_BK,
+                        0, fb);
+          } else if (mine) {
+            const int sh = p.row ? rsh : wshard;
+            const CUtensorMap* map = (h == 64) ? &p.tmW64[sh] : &p.tmW16[sh];
+            tma_load_2d(smem_u32(sW + (size_t)stage * SK_B_BYTES) + woff, map, kk * SK_BK,
+                        (int)wrow, fb);
+          }
+          __syncwarp();
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    });
+    // Every copy issued here is consumed by the MMA thread (same tile
+    // sequence); the epilogue waits for the commit that follows the last one.
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    SK_FOR_EACH_TILE(tl, {
+      if (ok && !mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u)) {
+        report_error(p.err, kErrTimeoutMma);
+        ok = false;
+      }
+      if (ok) {
+        tc_fence_after();
+        const int n = swiglu ? 2 * tl.rows : tl.rows;  // gate rows, then up rows
+        const uint32_t idesc = idesc_bf16_f32(128, n);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * SK_BN);
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase)) {
+            report_error(p.err, kErrTimeoutMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_sw128(smem_u32(sX + (size_t)stage * p.x_stage_bytes));
+          const uint64_t bdesc = sdesc_sw128(smem_u32(sW + (size_t)stage * SK_B_BYTES));
+#pragma unroll
+          for (int k = 0; k < SK_BK / SK_UMMA_K; ++k)
+            // advance the start address by k * 32 bytes inside the swizzle span
+            mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc,
+                     (kb > tl.kb0 || k > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&empty[stage]));  // stage reusable once these MMAs finish
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) mma_commit(smem_u32(&tfull[acc]));  // accumulator ready for the epilogue
+      }
+      if (++acc == SK_ACC_BUFS) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    });
+    // every MMA this thread issued has completed before TMEM is released
+    mma_commit(smem_u32(drain));
+    if (!mbar_wait_bounded(smem_u32(drain), 0)) report_error(p.err, kErrTimeoutDrain);
+  } else if (warp >= SK_EPI_WARP0) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                // TMEM lane quadrant this warp may access
+    const int64_t t = q * 32 + lane;       // this thread's token
+    const bool has_tokens = q * 32 < p.M;  // warp-uniform
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    SK_FOR_EACH_TILE(tl, {
+      if (ok) {
+        // all lanes wait, then agree: tcgen05.ld is warp-collective
+        ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) report_error(p.err, kErrTimeoutEpilogue);
+      }
+      if (ok) {
+        tc_fence_after();
+        const uint32_t taddr =
+            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * SK_BN);
+        if (has_tokens && p.row && p.cs > 1) {
+          // this rank's partial sum -> shared memory, for the cluster reduction
+          const int c = tl.pc[0].c;
+#pragma unroll 1
+          for (int j0 = 0; j0 < c; j0 += 8) {
+            float v[8];
+            tmem_ld8(taddr + (uint32_t)j0, v);
+            if (t < p.M) {
+              float4* dst = reinterpret_cast<float4*>(red + t * SK_RED_PITCH + j0);
+              dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+              dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+          }
+        } else if (has_tokens) {
+          for (int i = 0; i < tl.n; ++i) {
+            const Piece& pc = tl.pc[i];
+            const int64_t base = (p.row ? 0 : (int64_t)pc.shard * p.y_shard_stride) + t * p.ldy;
+            const float* bias = p.row ? p.bias[0] : (swiglu ? nullptr : p.bias[pc.shard]);
+#pragma unroll 1
+            for (int j0 = 0; j0 < pc.c; j0 += 8) {
+              float v[8];
+              tmem_ld8(taddr + (uint32_t)(pc.slot + j0), v);
+              const int valid = pc.c - j0 < 8 ? pc.c - j0 : 8;
+              if (swiglu) {
+                float u[8];
+                tmem_ld8(taddr + (uint32_t)(tl.rows + pc.slot + j0), u);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = act_silu(v[j]) * u[j];
+              } else {
+                if (bias) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    if (j < valid) v[j] += __ldg(bias + pc.loc + j0 + j);
+                }
+                if (!p.row && p.act == TP_ACT_GELU_ERF) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) v[j] = act_gelu_erf(v[j]);
+                }
+              }
+              if (t < p.M) store_row8(p.Y, p.ydt, base, pc.loc + j0, valid, v);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      }
+      if (++acc == SK_ACC_BUFS) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    });
+  }
+
+  __syncthreads();
+  if (p.row && p.cs > 1) {
+    // ---------------------------------------------------------- cluster reduction
+    // Every thread of every CTA of the cluster passes both barriers, whatever
+    // happened above.
+    cluster_sync_all();
+    const Tile tl = row_tile(p, rank);
+    const int c = tl.pc[0].c;
+    const int64_t loc = tl.pc[0].loc;
+    const int w = (SK_BN + p.cs - 1) / p.cs;  // outputs per rank
+    const int j_lo = rank * w;
+    const int j_hi = (int)imin((int64_t)j_lo + w, c);
+    const float* bias = p.bias[0];
+    const uint32_t red_s = smem_u32(red);
+    if (j_hi > j_lo) {
+      const int span = j_hi - j_lo;
+      const int64_t items = p.M * span;
+      for (int64_t it = threadIdx.x; it < items; it += SK_THREADS) {
+        const int64_t tok = it / span;
+        const int j = j_lo + (int)(it - tok * span);
+        const uint32_t off = (uint32_t)((tok * SK_RED_PITCH + j) * 4);
+        float sum = 0.0f;
+        for (int r = 0; r < p.cs; ++r) sum += dsmem_ld_f32(dsmem_addr(red_s + off, (uint32_t)r));
+        if (bias) sum += __ldg(bias + loc + j);
+        store_out(p.Y, p.ydt, tok * p.ldy + loc + j, sum);
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while a peer still reads its buffer
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, SK_TMEM_COLS);
+  }
+}
+
+#undef SK_FOR_EACH_TILE
+
+}  // namespace
+
+tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
+  if (p.xdt != TP_BF16 || p.M < 1 || p.M > kSkinnyMaxTokens) return TP_ERR_UNSUPPORTED;
+  SkinnyParams sp{};
+  sp.err = device_error_word();
+  if (!sp.err) return TP_ERR_CUDA;
+  const int xrows = (int)((p.M + 7) / 8 * 8);
+  const int64_t es = 2;
+  if (p.row) {
+    for (int i = 0; i < p.tp; ++i) {
+      const void* xi = static_cast<const char*>(p.X) + (int64_t)i * p.x_shard_off * es;
+      if (!make_tma_map_bf16(&sp.tmX[i], xi, (uint64_t)p.K, (uint64_t)p.M,
+                             (uint64_t)(p.ldx * es), (uint32_t)xrows))
+        return TP_ERR_CUDA;
+    }
+  } else if (!make_tma_map_bf16(&sp.tmX[0], p.X, (uint64_t)p.K, (uint64_t)p.M,
+                                (uint64_t)(p.ldx * es), (uint32_t)xrows)) {
+    return TP_ERR_CUDA;
+  }
+  for (int i = 0; i < p.tp; ++i) {
+    if (!make_tma_map_bf16(&sp.tmW16[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows,
+                           (uint64_t)(p.K * es), 16) ||
+        !make_tma_map_bf16(&sp.tmW64[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows,
+                           (uint64_t)(p.K * es), 64))
+      return TP_ERR_CUDA;
+  }
+  for (int i = 0; i < TP_MAX_TP; ++i) sp.bias[i] = p.bias[i];
+  sp.Y = p.Y;
+  sp.ldy = p.ldy;
+  sp.y_shard_stride = p.y_shard_stride;
+  sp.M = p.M;
+  sp.ns = p.ns;
+  sp.feat_total = p.row ? p.n_out : (int64_t)p.tp * p.ns;
+  sp.tp = p.tp;
+  sp.row = p.row ? 1 : 0;
+  sp.act = p.act;
+  sp.ydt = p.ydt;
+  sp.xrows = xrows;
+  sp.x_stage_bytes = xrows * SK_ROW_BYTES;
+  sp.kb_per_shard = (int)((p.K + SK_BK - 1) / SK_BK);
+  sp.kb_total = sp.kb_per_shard * (p.row ? p.tp : 1);
+
+  const int sms = sm_count();
+  int grid = 1;
+  sp.cs = 1;
+  if (p.row) {
+    // Output tiles of 256; clusters of cs CTAs split each tile's K loop so
+    // that tiles x cs fills the SMs (each CTA keeps at least one k-block).
+    const int64_t tiles = (p.n_out + SK_BN - 1) / SK_BN;
+    int64_t cs = std::max<int64_t>(1, std::min<int64_t>(SK_MAX_CLUSTER, sms / tiles));
+    cs = std::min<int64_t>(cs, sp.kb_total);
+    if (tiles * cs > INT32_MAX) return TP_ERR_BAD_SHAPE;
+    sp.cs = (int)cs;
+    grid = (int)(tiles * cs);
+  } else {
+    const int64_t units = (sp.feat_total + SK_GRAIN - 1) / SK_GRAIN;
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, sms));
+  }
+  const int avail = SK_SMEM_MAX - 1024 - SK_BAR_BYTES;
+  const int stages = std::min(SK_MAX_STAGES, avail / (sp.x_stage_bytes + SK_B_BYTES));
+  if (stages < 2) return TP_ERR_UNSUPPORTED;
+  sp.stages = stages;
+  const int ring = stages * (sp.x_stage_bytes + SK_B_BYTES);
+  // The MMA reads a full 128-row A tile from each X stage: the last one runs
+  // into the weight stages, which must be there.  The row side's reduction
+  // buffer reuses the ring.
+  if ((stages - 1) * sp.x_stage_bytes + SK_A_BYTES > ring) return TP_ERR_UNSUPPORTED;
+  if (p.row && sp.cs > 1 && (int64_t)xrows * SK_RED_PITCH * 4 > ring) return TP_ERR_UNSUPPORTED;
+  const int smem = 1024 + ring + SK_BAR_BYTES;
+
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SK_SMEM_MAX);
+  });
+  if (attr_err != cudaSuccess) return TP_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(SK_THREADS);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)sp.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, skinny_kernel, sp) != cudaSuccess) return TP_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // namespace tpla

@@ -1,9 +1,12 @@
 """GPU parity on small and ragged shapes: every entry point against the oracle.
 
 Shapes span several kernel tiles with ragged tails in M, N and K, every tp the
-pages use (1, 2, 4, 8) and some they do not (3), fp32 and bf16, each
-activation, with and without bias, on both kernels (weight-streaming GEMV for
-M <= 8, tcgen05 GEMM above).  All calls go through the C ABI.
+pages use (1, 2, 4, 8) and some they do not (3, 5), fp32 and bf16, each
+activation, with and without bias, on all three kernels: the weight-streaming
+GEMV (fp32, and bf16 with M <= 4), the tcgen05 decode kernel (bf16,
+5 <= M <= 128; the cases below put its per-SM feature ranges across shard and
+gate/up-group boundaries and give shards widths that are not multiples of 8)
+and the tcgen05 prefill GEMM (bf16, M > 128).  All calls go through the C ABI.
 """
 import numpy as np
 import pytest
@@ -62,6 +65,11 @@ COLUMN_CASES = [
     (5, 136, 300, 2, "swiglu", torch.bfloat16, False),
     (150, 264, 520, 4, "swiglu", torch.bfloat16, False),
     (333, 512, 1280, 2, "swiglu", torch.bfloat16, False),
+    (96, 200, 3000, 3, "swiglu", torch.bfloat16, False),   # partial gate/up groups
+    (64, 1000, 2600, 4, "gelu", torch.bfloat16, True),     # 650 outputs per shard
+    (16, 256, 40000, 2, "none", torch.bfloat16, False),    # several chunks per SM
+    (128, 64, 1000, 5, "none", torch.bfloat16, True),
+    (6, 72, 136, 1, "swiglu", torch.bfloat16, False),
 ]
 
 
@@ -126,6 +134,9 @@ ROW_CASES = [
     (130, 2048, 96, 8, torch.bfloat16, True),
     (257, 768, 520, 2, torch.bfloat16, True),
     (64, 4096, 256, 4, torch.bfloat16, False),
+    (100, 3000, 1000, 3, torch.bfloat16, True),   # K/tp = 1000: ragged k-block per shard
+    (128, 1024, 4000, 2, torch.bfloat16, False),
+    (5, 4096, 3000, 4, torch.bfloat16, True),
 ]
 
 
