@@ -51,7 +51,7 @@ tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream);
 // handful of tokens, up to kSkinnyMaxTokens).
 constexpr int64_t kSkinnyMaxTokens = 128;
 // bf16 calls with at most this many tokens go to the GEMV.
-constexpr int64_t kGemvMaxTokens = 4;
+constexpr int64_t kGemvMaxTokens = 2;
 tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream);
 
 // 2-D bf16 tensor map for TMA: `rows` rows of `inner` elements, row pitch

@@ -21,16 +21,17 @@
 //                     units of 8 (features numbered shard-major).  The range
 //                     is cut into pieces that stay inside one shard (and, for
 //                     SwiGLU, one gate/up group), and consecutive pieces are
-//                     packed at 8-row slots into B tiles of 256 weight rows,
-//                     so a CTA runs as few K loops as its bytes allow.  Every
+//                     packed at 16-row slots into one B tile of up to 512
+//                     weight rows (two MMAs of N <= 256 per k-step), so a CTA
+//                     normally runs a single K loop with every stage full.  Every
 //                     output accumulates over all of K in one TMEM column --
 //                     no split-K -- so its summation order depends on K only
 //                     and sharded results are bit-identical to tp = 1.
 //                     SwiGLU: a piece's gate rows sit at its slot among the
 //                     tile's first R rows and its up rows at the same slot
-//                     among the next R (R = slot rows of the tile, <= 128);
-//                     the MMA runs N = 2R and the thread that owns a token
-//                     reads gate column slot+j and up column R+slot+j.
+//                     among the next R (R = slot rows of the tile, <= 256);
+//                     the thread that owns a token reads gate column slot+j
+//                     and up column R+slot+j of the accumulator.
 //   row-parallel:     Y = sum_i X_i . W_i^T + b.  The outputs are cut into
 //                     tiles of 256; each tile belongs to a thread-block
 //                     cluster of cs CTAs that split the K loop (shard 0's
@@ -50,10 +51,11 @@
 //               the tile's weight rows as 64-row and 16-row boxes, one box
 //               per lane: a single thread issuing many small boxes cannot
 //               keep the TMA unit busy.
-//   warp 1      TMEM allocation (512 columns: two 128 x 256 fp32 accumulators)
-//               and the single thread issuing tcgen05.mma (M=128, N<=256,
-//               K=16), committing each stage back to the producer and each
-//               finished chunk to the epilogue.
+//   warp 1      TMEM allocation (512 columns: one accumulator of up to 512
+//               fp32 columns, or two when they fit) and the single thread
+//               issuing tcgen05.mma (M=128, N<=256, K=16), committing each
+//               stage back to the producer and each finished tile to the
+//               epilogue.
 //   warps 2-5   epilogue: tcgen05.ld (one TMEM lane = one token per thread),
 //               bias / activation in fp32, one rounding, row stores; on the
 //               row side the partial goes to shared memory for the cluster
@@ -81,11 +83,11 @@ constexpr int SK_BK = 64;                   // k per stage: one 128-byte swizzle
 constexpr int SK_UMMA_K = 16;
 constexpr int SK_ROW_BYTES = SK_BK * 2;     // 128 bytes per staged row
 constexpr int SK_A_BYTES = 128 * SK_ROW_BYTES;  // the A tile one MMA reads (128 rows)
-constexpr int SK_BN = 256;                  // weight rows per B tile (MMA N)
-constexpr int SK_B_BYTES = SK_BN * SK_ROW_BYTES;  // 32 KB
+constexpr int SK_BN = 256;                  // weight rows per MMA (its N, at most)
+constexpr int SK_TILE_ROWS_MAX = 512;       // weight rows of one B tile (two MMAs)
 constexpr int SK_MAX_STAGES = 16;
-constexpr int SK_ACC_BUFS = 2;
-constexpr int SK_TMEM_COLS = SK_ACC_BUFS * SK_BN;
+constexpr int SK_ACC_BUFS = 2;              // accumulator buffers, when two fit in TMEM
+constexpr int SK_TMEM_COLS = 512;
 constexpr int SK_GRAIN = 16;                // features per balance unit (column side)
 constexpr int SK_MAX_BOXES = 31;            // weight boxes per stage (one per producer lane)
 constexpr int SK_MAX_CLUSTER = 8;
@@ -94,7 +96,7 @@ constexpr int SK_NUM_BARS = 2 * SK_MAX_STAGES + 2 * SK_ACC_BUFS + 1;
 constexpr int SK_BAR_BYTES = SK_NUM_BARS * 8 + 16;
 constexpr int SK_SMEM_MAX = 232448;         // dynamic shared memory per CTA (227 KB)
 constexpr int64_t G = TP_GATE_UP_GROUP;
-static_assert(2 * G == SK_BN, "a SwiGLU chunk's gate and up rows fill one B tile");
+static_assert(2 * G == SK_BN, "a gate/up group's rows fill one MMA");
 
 struct SkinnyParams {
   CUtensorMap tmX[TP_MAX_TP];    // column: [0] = X; row: X_i.  Box {64, xrows}.
@@ -107,6 +109,9 @@ struct SkinnyParams {
   int64_t M, ns, feat_total;     // feat_total: column tp*ns; row n_out
   int tp, row, act, ydt;
   int xrows, x_stage_bytes, stages;
+  int w_stage_bytes;             // weight rows of a B tile x 128 bytes
+  int tile_cap;                  // column: features (SwiGLU) or rows per tile
+  int acc_stride, acc_bufs;      // TMEM columns per accumulator buffer, buffers
   int kb_per_shard, kb_total;
   int cs;                        // row side: CTAs per cluster splitting K
 };
@@ -163,7 +168,7 @@ __device__ __forceinline__ bool tile_box(const Tile& t, bool swiglu, int want, i
 // advances f past the features it takes.
 __device__ __forceinline__ Tile column_tile(const SkinnyParams& p, int64_t& f, int64_t f1) {
   const bool swiglu = p.act == TP_ACT_SWIGLU;
-  const int cap = swiglu ? (int)G : SK_BN;  // slot rows per tile (features for SwiGLU)
+  const int cap = p.tile_cap;  // slot rows per tile (features for SwiGLU)
   Tile t;
   t.n = 0;
   t.rows = 0;
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const int S = p.stages;
   uint8_t* sX = smem;                                      // S x-stages, then
   uint8_t* sW = smem + (size_t)S * p.x_stage_bytes;        // S weight stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sW + (size_t)S * SK_B_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sW + (size_t)S * p.w_stage_bytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + SK_MAX_STAGES;
   uint64_t* tfull = bars + 2 * SK_MAX_STAGES;
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int a = 0; a < SK_ACC_BUFS; ++a) {
+    for (int a = 0; a < p.acc_bufs; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
       mbar_init(smem_u32(&tempty[a]), 4);  // one arrive per epilogue warp
     }
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           } else if (mine) {
             const int sh = p.row ? rsh : wshard;
             const CUtensorMap* map = (h == 64) ? &p.tmW64[sh] : &p.tmW16[sh];
-            tma_load_2d(smem_u32(sW + (size_t)stage * SK_B_BYTES) + woff, map, kk * SK_BK,
+            tma_load_2d(smem_u32(sW + (size_t)stage * p.w_stage_bytes) + woff, map, kk * SK_BK,
                         (int)wrow, fb);
           }
           __syncwarp();
@@ -359,9 +364,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       }
       if (ok) {
         tc_fence_after();
-        const int n = swiglu ? 2 * tl.rows : tl.rows;  // gate rows, then up rows
-        const uint32_t idesc = idesc_bf16_f32(128, n);
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * SK_BN);
+        const int nrows = swiglu ? 2 * tl.rows : tl.rows;  // gate rows, then up rows
+        const int n0 = nrows < SK_BN ? nrows : SK_BN;        // first MMA's N
+        const int n1 = nrows - n0;                           // second MMA's N (or 0)
+        const uint32_t idesc0 = idesc_bf16_f32(128, n0);
+        const uint32_t idesc1 = idesc_bf16_f32(128, n1 > 0 ? n1 : 16);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
         for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase)) {
             report_error(p.err, kErrTimeoutMma);
@@ -370,12 +378,20 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           }
           tc_fence_after();
           const uint64_t adesc = sdesc_sw128(smem_u32(sX + (size_t)stage * p.x_stage_bytes));
-          const uint64_t bdesc = sdesc_sw128(smem_u32(sW + (size_t)stage * SK_B_BYTES));
+          const uint32_t wbase = smem_u32(sW + (size_t)stage * p.w_stage_bytes);
+          const uint64_t bdesc0 = sdesc_sw128(wbase);
+          const uint64_t bdesc1 = sdesc_sw128(wbase + SK_BN * SK_ROW_BYTES);
 #pragma unroll
-          for (int k = 0; k < SK_BK / SK_UMMA_K; ++k)
-            // advance the start address by k * 32 bytes inside the swizzle span
-            mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc,
-                     (kb > tl.kb0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < SK_BK / SK_UMMA_K; ++k) {
+            // advance the start address by k * 32 bytes inside the swizzle span;
+            // B rows [0, 256) feed accumulator columns [0, 256), rows [256, ..)
+            // columns [256, ..)
+            const uint32_t accum = (kb > tl.kb0 || k > 0) ? 1u : 0u;
+            mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc0 + (uint64_t)(k * 2), idesc0, accum);
+            if (n1 > 0)
+              mma_bf16(d_tmem + SK_BN, adesc + (uint64_t)(k * 2), bdesc1 + (uint64_t)(k * 2),
+                       idesc1, accum);
+          }
           mma_commit(smem_u32(&empty[stage]));  // stage reusable once these MMAs finish
           if (++stage == S) {
             stage = 0;
@@ -384,7 +400,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         }
         if (ok) mma_commit(smem_u32(&tfull[acc]));  // accumulator ready for the epilogue
       }
-      if (++acc == SK_ACC_BUFS) {
+      if (++acc == p.acc_bufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -410,7 +426,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
       if (ok) {
         tc_fence_after();
         const uint32_t taddr =
-            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * SK_BN);
+            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.acc_stride);
         if (has_tokens && p.row && p.cs > 1) {
           // this rank's partial sum -> shared memory, for the cluster reduction
           const int c = tl.pc[0].c;
@@ -458,7 +474,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
       }
-      if (++acc == SK_ACC_BUFS) {
+      if (++acc == p.acc_bufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -562,13 +578,27 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
     const int64_t units = (sp.feat_total + SK_GRAIN - 1) / SK_GRAIN;
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, sms));
   }
+  // B tile: the row side's 256 outputs; on the column side as many features
+  // (rows) as the widest CTA range, up to 256 (SwiGLU: gate + up rows).
+  const bool swiglu = !p.row && p.act == TP_ACT_SWIGLU;
+  int tile_rows = SK_BN;
+  if (!p.row) {
+    const int64_t units = (sp.feat_total + SK_GRAIN - 1) / SK_GRAIN;
+    const int64_t max_range = (units + grid - 1) / grid * SK_GRAIN;
+    sp.tile_cap = (int)std::min<int64_t>(SK_BN, max_range);
+    tile_rows = swiglu ? 2 * sp.tile_cap : sp.tile_cap;
+  }
+  sp.w_stage_bytes = tile_rows * SK_ROW_BYTES;
+  sp.acc_stride = (tile_rows + 31) / 32 * 32;
+  sp.acc_bufs = (SK_ACC_BUFS * sp.acc_stride <= SK_TMEM_COLS) ? SK_ACC_BUFS : 1;
   const int avail = SK_SMEM_MAX - 1024 - SK_BAR_BYTES;
-  const int stages = std::min(SK_MAX_STAGES, avail / (sp.x_stage_bytes + SK_B_BYTES));
+  const int stages = std::min(SK_MAX_STAGES, avail / (sp.x_stage_bytes + sp.w_stage_bytes));
   if (stages < 2) return TP_ERR_UNSUPPORTED;
   sp.stages = stages;
-  const int ring = stages * (sp.x_stage_bytes + SK_B_BYTES);
-  // The MMA reads a full 128-row A tile from each X stage: the last one runs
-  // into the weight stages, which must be there.  The row side's reduction
+  const int ring = stages * (sp.x_stage_bytes + sp.w_stage_bytes);
+  // The MMA reads a full 128-row A tile from each X stage: the read past the
+  // last X stage runs into the weight stages, which must be there.  (It reads
+  // only the tile's rows from a weight stage.)  The row side's reduction
   // buffer reuses the ring.
   if ((stages - 1) * sp.x_stage_bytes + SK_A_BYTES > ring) return TP_ERR_UNSUPPORTED;
   if (p.row && sp.cs > 1 && (int64_t)xrows * SK_RED_PITCH * 4 > ring) return TP_ERR_UNSUPPORTED;

@@ -3,8 +3,8 @@
 Shapes span several kernel tiles with ragged tails in M, N and K, every tp the
 pages use (1, 2, 4, 8) and some they do not (3, 5), fp32 and bf16, each
 activation, with and without bias, on all three kernels: the weight-streaming
-GEMV (fp32, and bf16 with M <= 4), the tcgen05 decode kernel (bf16,
-5 <= M <= 128; the cases below put its per-SM feature ranges across shard and
+GEMV (fp32, and bf16 with M <= 2), the tcgen05 decode kernel (bf16,
+3 <= M <= 128; the cases below put its per-SM feature ranges across shard and
 gate/up-group boundaries and give shards widths that are not multiples of 8)
 and the tcgen05 prefill GEMM (bf16, M > 128).  All calls go through the C ABI.
 """
@@ -54,6 +54,7 @@ COLUMN_CASES = [
     (5, 64, 48, 3, "gelu", torch.float32, True),
     (20, 32, 16, 4, "gelu", torch.float32, False),
     (1, 64, 96, 2, "gelu", torch.bfloat16, True),
+    (2, 264, 136, 2, "swiglu", torch.bfloat16, False),
     (3, 520, 200, 4, "gelu", torch.bfloat16, True),
     (8, 256, 384, 8, "none", torch.bfloat16, False),
     (128, 64, 256, 1, "none", torch.bfloat16, False),      # exactly one GEMM tile
