@@ -77,7 +77,7 @@ tp_status run(const LinearProblem& p, cudaStream_t s) {
   if (p.M == 0) return TP_OK;
   if (p.xdt == TP_BF16 && p.M > kGemvMaxTokens) {
     if (p.M <= kSkinnyMaxTokens) return launch_skinny(p, s);
-    return launch_gemm_tc(p, s);
+    return launch_gemm_pair(p, s);
   }
   return launch_gemv(p, s);
 }

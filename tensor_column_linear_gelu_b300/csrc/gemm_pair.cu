@@ -1,5 +1,5 @@
-// gemm_tc.cu -- tcgen05 / TMEM tensor-core GEMM fed by TMA, for bf16 calls
-// with many tokens (prefill-shaped).
+// gemm_pair.cu -- tcgen05 / TMEM tensor-core GEMM on CTA pairs, fed by TMA,
+// for bf16 calls with many tokens (prefill-shaped).
 //
 //   column-parallel:  Y_i = act(X . W_i^T + b_i) for every shard i in one launch;
 //                     the shard index is a group of N-tiles, shard i's tiles
@@ -15,27 +15,33 @@
 // Parallelism Works Under the Hood"; "Tensor parallel serving",
 // "Column-parallel and row-parallel layers, paired".)
 //
-// Structure (one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer: A (activations) and B (weights) k-blocks of
-//               64 bf16 (one 128-byte swizzle span) into a 4-stage ring.
-//   warp 1      TMEM allocation (512 columns: two 128x256 fp32 accumulators)
-//               and the single thread that issues tcgen05.mma (M=128, N=256,
-//               K=16, bf16 x bf16 -> fp32), committing each stage back to the
-//               producer and each finished tile to the epilogue.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
-//               output row per thread), bias / activation in fp32, one
-//               rounding to the output dtype, stores.  Double buffering lets
-//               the epilogue of tile t overlap the mainloop of tile t+1.
+// Structure: clusters of two CTAs (a pair), persistent over 256 x 256 output
+// tiles.  One MMA (tcgen05.mma.cta_group::2, M=256, N=256, K=16) covers the
+// pair's tile: the even CTA issues it, each CTA holds 128 of the tile's rows
+// of A (tokens) and 128 of its rows of B (weights) in shared memory, and
+// each CTA's TMEM holds the accumulator of its 128 token rows.  Per SM this
+// halves the weight bytes loaded and read per FLOP compared with a 128 x 256
+// tile on one SM.
+//   warp 0      TMA producer (both CTAs): this CTA's A and B halves of each
+//               64-wide k-block into a 6-stage ring; completion is counted on
+//               the even CTA's barrier, which expects both halves.
+//   warp 1      TMEM allocation (both CTAs, collectively) and, in the even
+//               CTA, the single thread that issues the MMAs, committing each
+//               stage back to both producers and each finished tile to both
+//               epilogues (multicast commits).
+//   warps 2-5   epilogue (both CTAs): tcgen05.ld of this CTA's accumulator
+//               rows (one TMEM lane = one token row per thread), bias /
+//               activation in fp32, one rounding, stores; then an arrive on
+//               the even CTA's accumulator-free barrier.
 // Every mbarrier wait is bounded (sync.cuh); a wait that gives up records the
-// failure in the device error word, raises a CTA-wide abort flag, and every
-// role unwinds: in-flight TMA copies and MMAs are waited for (with a limit)
-// and TMEM is freed before the CTA exits.
+// failure in the device error word, raises the CTA's abort flag, and the
+// roles unwind.  Every thread of both CTAs reaches the closing cluster
+// barrier and the collective TMEM release whatever happened.
 //
 // Summation order of an output element: k-blocks in increasing k (then, on
 // the row side, shard by shard), 4 MMAs of K=16 per k-block.  It does not
 // depend on N or tp, so column-parallel outputs are bit-identical to tp = 1.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <mutex>
@@ -48,27 +54,29 @@
 namespace tpla {
 namespace {
 
-constexpr int BM = 128;   // tokens per tile (TMEM lanes)
-constexpr int BN = 256;   // output columns per tile (MMA N)
-constexpr int BK = 64;    // k per stage: 64 bf16 = 128 bytes = one swizzle span
+constexpr int PM = 256;             // tokens per pair tile (MMA M)
+constexpr int HM = PM / 2;          // tokens per CTA (TMEM lanes)
+constexpr int PN = 256;             // output columns per tile (MMA N)
+constexpr int HN = PN / 2;          // weight rows of B per CTA
+constexpr int BK = 64;              // k per stage: 64 bf16 = 128 bytes = one swizzle span
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGES = 6;
+constexpr int A_BYTES = HM * BK * 2;  // 16 KB
+constexpr int B_BYTES = HN * BK * 2;  // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_BUFS = 2;
-constexpr int TMEM_COLS = 512;        // ACC_BUFS x BN fp32 columns
+constexpr int TMEM_COLS = 512;      // ACC_BUFS x PN fp32 columns
 constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
 constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
 constexpr int64_t G = TP_GATE_UP_GROUP;
-static_assert(2 * G == BN, "a SwiGLU tile holds one gate/up group");
+static_assert(2 * G == PN, "a SwiGLU tile holds one gate/up group");
 static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 
-struct alignas(64) GemmParams {
-  CUtensorMap tmA[TP_MAX_TP];  // column: [0] = X; row: X_i
-  CUtensorMap tmB[TP_MAX_TP];  // W_i
+struct PairParams {
+  CUtensorMap tmA[TP_MAX_TP];  // column: [0] = X; row: X_i.  Box {64, 128}.
+  CUtensorMap tmB[TP_MAX_TP];  // W_i.  Box {64, 128}.
   const float* bias[TP_MAX_TP];
   void* Y;
   unsigned int* err;
@@ -86,45 +94,48 @@ __device__ __forceinline__ int valid_count(int64_t limit, int64_t n) {
 
 struct TileCoord {
   int shard;   // column: shard of this tile; row: unused
-  int64_t m0;  // first token
+  int64_t m0;  // first token of the pair's tile
   int64_t n0;  // first row of W_i (column) or first output column (row)
 };
 
-// Tiles are numbered M-fastest: the CTAs running at the same time share the
+// Tiles are numbered M-fastest: the pairs running at the same time share the
 // weight tile(s) they stream and keep the activations in L2.
-__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int tile) {
+__device__ __forceinline__ TileCoord tile_coord(const PairParams& p, int tile) {
   const int mt = tile % p.m_tiles;
   const int nt = tile / p.m_tiles;
   TileCoord c;
-  c.m0 = (int64_t)mt * BM;
+  c.m0 = (int64_t)mt * PM;
   if (p.row) {
     c.shard = 0;
-    c.n0 = (int64_t)nt * BN;
+    c.n0 = (int64_t)nt * PN;
   } else {
     c.shard = nt / p.n_tiles_per_shard;
-    c.n0 = (int64_t)(nt % p.n_tiles_per_shard) * BN;
+    c.n0 = (int64_t)(nt % p.n_tiles_per_shard) * PN;
   }
   return c;
 }
 
-// ---------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ PairParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + ACC_BUFS;
-  uint64_t* drain = bars + 2 * STAGES + 2 * ACC_BUFS;
+  uint64_t* full = bars;                 // even CTA's are used: both halves land there
+  uint64_t* empty = bars + STAGES;       // each CTA's own: its producer waits on it
+  uint64_t* tfull = bars + 2 * STAGES;   // each CTA's own: its epilogue waits on it
+  uint64_t* tempty = tfull + ACC_BUFS;   // even CTA's: both epilogues arrive
+  uint64_t* drain = tempty + ACC_BUFS;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS) + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: even CTA of the pair, 1: odd
+  const bool lead = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -133,7 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     }
     for (int a = 0; a < ACC_BUFS; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), 4);  // one arrive per epilogue warp
+      mbar_init(smem_u32(&tempty[a]), 8);  // one arrive per epilogue warp of both CTAs
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -144,11 +155,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     for (int i = 0; i < nmaps; ++i) prefetch_tmap(&p.tmA[i]);
     for (int i = 0; i < p.tp; ++i) prefetch_tmap(&p.tmB[i]);
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
-  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
+  // Both CTAs' barriers are initialised and the TMEM address is known before
+  // any copy, MMA or remote arrive targets them.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -156,11 +167,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t last_parity[STAGES];
-    bool issued[STAGES];
-    for (int s = 0; s < STAGES; ++s) issued[s] = false;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+    for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
       const TileCoord c = tile_coord(p, tile);
       for (int kb = 0; kb < p.kb_total; ++kb) {
         const int sh = p.row ? kb / p.kb_per_shard : c.shard;
@@ -171,39 +179,38 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           ok = false;
           break;
         }
-        const uint32_t fb = smem_u32(&full[stage]);
-        mbar_arrive_expect_tx(fb, STAGE_BYTES);
-        tma_load_2d(smem_u32(sA + stage * A_BYTES), &p.tmA[p.row ? sh : 0], kk * BK, (int)c.m0, fb);
-        tma_load_2d(smem_u32(sB + stage * B_BYTES), &p.tmB[p.row ? sh : c.shard], kk * BK,
-                    (int)c.n0, fb);
-        issued[stage] = true;
-        last_parity[stage] = phase;
+        const uint32_t fb_own = smem_u32(&full[stage]);
+        const uint32_t fb = dsmem_addr(fb_own, 0);  // the even CTA's barrier
+        if (lead) mbar_arrive_expect_tx(fb_own, 2 * STAGE_BYTES);
+        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &p.tmA[p.row ? sh : 0], kk * BK,
+                         (int)(c.m0 + (int64_t)rank * HM), fb);
+        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &p.tmB[p.row ? sh : c.shard], kk * BK,
+                         (int)(c.n0 + (int64_t)rank * HN), fb);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // wait (bounded) for every copy this thread started, so none lands after exit
-    for (int s = 0; s < STAGES; ++s)
-      if (issued[s] && !mbar_wait_bounded(smem_u32(&full[s]), last_parity[s], kWaitLimitNs))
-        report_error(p.err, kErrTimeoutDrain);
-  } else if (warp == 1 && lane == 0) {
+    // Every copy issued here is consumed by an MMA (the even CTA issues them
+    // for the same tile sequence), and this CTA's epilogue waits for the
+    // commit that follows the last one; the closing cluster barrier follows.
+  } else if (warp == 1 && lane == 0 && lead) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+    constexpr uint32_t IDESC = idesc_bf16_f32(PM, PN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+    for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
       if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
         report_error(p.err, kErrTimeoutMma);
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PN);
       for (int kb = 0; kb < p.kb_total; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs, abort_flag)) {
           report_error(p.err, kErrTimeoutMma);
@@ -217,33 +224,34 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k) {
           // advance the start address by k * 32 bytes inside the swizzle span
-          mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), IDESC,
-                   (kb > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_pair(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), IDESC,
+                        (kb > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(smem_u32(&empty[stage]));  // stage reusable once these MMAs finish
+        mma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);  // both producers may refill
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      mma_commit(smem_u32(&tfull[acc]));      // accumulator ready for the epilogue
+      mma_commit_pair_mc(smem_u32(&tfull[acc]), 0x3);  // both epilogues may read
       if (++acc == ACC_BUFS) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
     // every MMA this thread issued has completed before TMEM is released
-    mma_commit(smem_u32(drain));
+    mma_commit_pair(smem_u32(drain));
     if (!mbar_wait_bounded(smem_u32(drain), 0, kWaitLimitNs)) report_error(p.err, kErrTimeoutDrain);
   } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quadrant this warp may access
-    const int row_in_tile = q * 32 + lane;
+    const int row_in_tile = (int)rank * HM + q * 32 + lane;
     const bool swiglu = (!p.row && p.act == TP_ACT_SWIGLU);
+    const uint32_t tempty_lead = dsmem_addr(smem_u32(&tempty[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int tile = pair; tile < p.num_tiles; tile += npairs) {
       // all lanes wait, then agree: tcgen05.ld below is warp-collective, so
       // the warp must never split on a timeout
       bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, kWaitLimitNs, abort_flag);
@@ -257,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       const TileCoord c = tile_coord(p, tile);
       const int64_t m = c.m0 + row_in_tile;
       const bool row_ok = m < p.M;
-      const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * PN);
       if (swiglu) {
         // tile = one packed group: gate columns [0,128), up columns [128,256)
         const int64_t out0 = (c.n0 / (2 * G)) * G;   // first output of the group (shard-local)
@@ -275,11 +283,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         }
       } else {
         const int64_t limit = p.row ? p.n_out : p.ns;
-        const int64_t base =
-            (p.row ? 0 : (int64_t)c.shard * p.y_shard_stride) + m * p.ldy;
+        const int64_t base = (p.row ? 0 : (int64_t)c.shard * p.y_shard_stride) + m * p.ldy;
         const float* bias = p.row ? p.bias[0] : p.bias[c.shard];
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ++ch) {
+        for (int ch = 0; ch < PN / 32; ++ch) {
           float v[32];
           tmem_ld32(trow + ch * 32, v);
           const int64_t n = c.n0 + ch * 32;
@@ -298,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (lane == 0) mbar_arrive_cluster(tempty_lead + (uint32_t)(acc * 8));
       if (++acc == ACC_BUFS) {
         acc = 0;
         acc_phase ^= 1u;
@@ -307,62 +314,36 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   }
 
   __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
+  // No CTA of the pair leaves (or frees TMEM) while the other may still arrive
+  // on its barriers or while MMAs may still write its TMEM: the even CTA's
+  // MMA thread has waited for its last MMA before this barrier.
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 }  // namespace
 
-// ---------------------------------------------------------------- host side
-namespace {
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-}  // namespace
-
-bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                       uint64_t ld_bytes, uint32_t box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {ld_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream) {
-  GemmParams gp{};
+tp_status launch_gemm_pair(const LinearProblem& p, cudaStream_t stream) {
+  PairParams gp{};
   gp.err = device_error_word();
   if (!gp.err) return TP_ERR_CUDA;
   const int64_t es = 2;
   if (p.row) {
     for (int i = 0; i < p.tp; ++i) {
       const void* xi = static_cast<const char*>(p.X) + (int64_t)i * p.x_shard_off * es;
-      if (!make_tma_map_bf16(&gp.tmA[i], xi, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
+      if (!make_tma_map_bf16(&gp.tmA[i], xi, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es),
+                             HM))
         return TP_ERR_CUDA;
     }
-  } else {
-    if (!make_tma_map_bf16(&gp.tmA[0], p.X, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es), BM))
-      return TP_ERR_CUDA;
+  } else if (!make_tma_map_bf16(&gp.tmA[0], p.X, (uint64_t)p.K, (uint64_t)p.M,
+                                (uint64_t)(p.ldx * es), HM)) {
+    return TP_ERR_CUDA;
   }
   for (int i = 0; i < p.tp; ++i)
-    if (!make_tma_map_bf16(&gp.tmB[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows, (uint64_t)(p.K * es), BN))
+    if (!make_tma_map_bf16(&gp.tmB[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows,
+                           (uint64_t)(p.K * es), HN))
       return TP_ERR_CUDA;
   for (int i = 0; i < TP_MAX_TP; ++i) gp.bias[i] = p.bias[i];
   gp.Y = p.Y;
@@ -375,14 +356,14 @@ tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream) {
   gp.row = p.row ? 1 : 0;
   gp.act = p.act;
   gp.ydt = p.ydt;
-  gp.m_tiles = (int)((p.M + BM - 1) / BM);
+  gp.m_tiles = (int)((p.M + PM - 1) / PM);
   gp.kb_per_shard = (int)((p.K + BK - 1) / BK);
   if (p.row) {
-    gp.n_tiles_per_shard = (int)((p.n_out + BN - 1) / BN);
+    gp.n_tiles_per_shard = (int)((p.n_out + PN - 1) / PN);
     gp.n_tiles = gp.n_tiles_per_shard;
     gp.kb_total = gp.kb_per_shard * p.tp;
   } else {
-    gp.n_tiles_per_shard = (int)((p.w_rows + BN - 1) / BN);
+    gp.n_tiles_per_shard = (int)((p.w_rows + PN - 1) / PN);
     gp.n_tiles = gp.n_tiles_per_shard * p.tp;
     gp.kb_total = gp.kb_per_shard;
   }
@@ -393,12 +374,24 @@ tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return TP_ERR_CUDA;
-  const int grid = (int)std::min<int64_t>(tiles, sm_count());
-  gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(gp);
+  const int pairs = (int)std::min<int64_t>(tiles, sm_count() / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * std::max(pairs, 1)));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = (size_t)SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemm_pair_kernel, gp) != cudaSuccess) return TP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 

@@ -44,8 +44,9 @@ struct LinearProblem {
 // Weight-streaming GEMV on CUDA cores (few tokens; also the fp32 path).
 tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream);
 
-// tcgen05 / TMEM tensor-core GEMM fed by TMA (bf16; many tokens).
-tp_status launch_gemm_tc(const LinearProblem& p, cudaStream_t stream);
+// tcgen05 / TMEM tensor-core GEMM fed by TMA on CTA pairs (bf16; many
+// tokens; 256 x 256 tiles).
+tp_status launch_gemm_pair(const LinearProblem& p, cudaStream_t stream);
 
 // tcgen05 decode kernel with the weights as the MMA's M operand (bf16; a
 // handful of tokens, up to kSkinnyMaxTokens).
