@@ -98,11 +98,19 @@ struct TileCoord {
   int64_t n0;  // first row of W_i (column) or first output column (row)
 };
 
-// Tiles are numbered M-fastest: the pairs running at the same time share the
-// weight tile(s) they stream and keep the activations in L2.
+// Tiles are numbered M-fastest within groups of up to GROUP_M m-tiles, and the
+// groups are swept one after the other: the pairs running at the same time
+// share the weight tiles they stream, and a group's activations (2048 tokens)
+// stay in L2 while the weights pass through.
+constexpr int GROUP_M = 8;
 __device__ __forceinline__ TileCoord tile_coord(const PairParams& p, int tile) {
-  const int mt = tile % p.m_tiles;
-  const int nt = tile / p.m_tiles;
+  const int per_group = GROUP_M * p.n_tiles;
+  const int g = tile / per_group;
+  const int m_first = g * GROUP_M;
+  const int gm = min(GROUP_M, p.m_tiles - m_first);  // m-tiles in this group
+  const int t = tile - g * per_group;
+  const int mt = m_first + t % gm;
+  const int nt = t / gm;
   TileCoord c;
   c.m0 = (int64_t)mt * PM;
   if (p.row) {

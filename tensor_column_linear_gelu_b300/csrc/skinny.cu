@@ -297,6 +297,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    // X is re-read by every SM; the weights are streamed once.
+    const uint64_t pol_x = l2_policy_evict_last();
+    const uint64_t pol_w = l2_policy_evict_first();
     SK_FOR_EACH_TILE(tl, {
       if (ok) {
         int piece = 0, half = 0, r = 0, h = 0;
@@ -332,13 +335,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           const uint32_t fb = smem_u32(&full[stage]);
           if (lane == 0) {
             mbar_arrive_expect_tx(fb, bytes);
-            tma_load_2d(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh], kk * SK_BK,
-                        0, fb);
+            tma_load_2d_hint(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh], kk * SK_BK,
+                        0, fb, pol_x);
           } else if (mine) {
             const int sh = p.row ? rsh : wshard;
             const CUtensorMap* map = (h == 64) ? &p.tmW64[sh] : &p.tmW16[sh];
-            tma_load_2d(smem_u32(sW + (size_t)stage * p.w_stage_bytes) + woff, map, kk * SK_BK,
-                        (int)wrow, fb);
+            tma_load_2d_hint(smem_u32(sW + (size_t)stage * p.w_stage_bytes) + woff, map, kk * SK_BK,
+                        (int)wrow, fb, pol_w);
           }
           __syncwarp();
           if (++stage == S) {
