@@ -62,7 +62,7 @@ _i64 = ctypes.c_int64
 
 
 def _bind(lib):
-    for name in ("orc_gelu", "orc_silu", "orc_round_bf16"):
+    for name in ("orc_gelu", "orc_silu", "orc_round_bf16", "orc_round_f32"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_double
         fn.argtypes = [ctypes.c_double]
@@ -77,6 +77,8 @@ def _bind(lib):
         _f, ctypes.c_int, _d, _i64]
     lib.orc_row_parallel.argtypes = [ctypes.c_int, _i64, _i64, _i64, _f, _i64, _f,
                                      _i64, _f, _d, _i64]
+    lib.orc_row_parallel_ring.argtypes = [ctypes.c_int, _i64, _i64, _i64, _f, _i64, _f,
+                                          _i64, _f, ctypes.c_int, _d, _i64]
     lib.orc_mlp_block.argtypes = [ctypes.c_int, _i64, _i64, _i64, ctypes.c_int, _f,
                                   _f, _f, _f, _f, _f, ctypes.c_int, _d, _d]
     lib.orc_qkv_proj.argtypes = [ctypes.c_int, _i64, _i64, ctypes.c_int,
@@ -84,7 +86,8 @@ def _bind(lib):
     lib.orc_o_proj.argtypes = [ctypes.c_int, _i64, _i64, ctypes.c_int, ctypes.c_int,
                                _f, _f, _f, _d]
     for name in ("orc_linear", "orc_swiglu", "orc_column_parallel",
-                 "orc_column_parallel_uneven", "orc_row_parallel", "orc_mlp_block",
+                 "orc_column_parallel_uneven", "orc_row_parallel", "orc_row_parallel_ring",
+                 "orc_mlp_block",
                  "orc_qkv_proj", "orc_o_proj"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -193,6 +196,23 @@ class Oracle:
         _check(self._lib.orc_row_parallel(tp, M, K, N, _pf(X), K, _pf(W), K, _pf(b),
                                           _pd(Y), N), "row_parallel")
         return Y
+
+    def row_parallel_ring(self, tp, X, W, b=None, wire="bf16"):
+        """Row split whose all-reduce adds the partials as a ring all-reduce does:
+        partials held in the wire dtype, chunk c summed from rank c around the
+        ring, rounded to the wire dtype after every hop, + b once (fp64 out)."""
+        X, W, b = _f32(X), _f32(W), _f32(b)
+        M, K = X.shape
+        N = W.shape[0]
+        assert W.shape[1] == K and wire in ("bf16", "f32")
+        Y = np.empty((M, N), dtype=np.float64)
+        _check(self._lib.orc_row_parallel_ring(tp, M, K, N, _pf(X), K, _pf(W), K, _pf(b),
+                                               1 if wire == "bf16" else 0, _pd(Y), N),
+               "row_parallel_ring")
+        return Y
+
+    def round_f32(self, x: float) -> float:
+        return self._lib.orc_round_f32(float(x))
 
     def mlp_block(self, tp, X, W1, b1, W2, b2, act="gelu", W1u=None, round_h=True):
         """FFN block: column (act per shard) -> [bf16 h] -> row (+ b2 once).

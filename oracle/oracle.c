@@ -265,6 +265,68 @@ int orc_row_parallel(int tp, int64_t M, int64_t K, int64_t N, const float* X,
   return ORC_OK;
 }
 
+/* Round an fp64 value to the nearest fp32 value (ties to even). */
+double orc_round_f32(double x) { return (double)(float)x; }
+
+/*
+ * Row-parallel linear whose all-reduce adds the partials the way a ring
+ * all-reduce does on real devices [P3 RowParallelLinear (dist.all_reduce SUM
+ * of each rank's local partial, then + bias); P5 "Communication cost" (the
+ * ring all-reduce: the message is cut into p chunks, each chunk's running sum
+ * travels once around the ring in the reduce-scatter, the all-gather copies
+ * the finished chunks)].
+ *
+ * Readings where the pages leave the arithmetic open:
+ *   - each rank holds its partial Y_i = X_i . W_i^T in the wire dtype (fp32,
+ *     or bf16 rounded to nearest even) before the collective;
+ *   - every hop sends the running sum in the wire dtype, so the sum is rounded
+ *     to the wire dtype after each addition;
+ *   - the flattened message of L = M*N elements is cut into p chunks, chunk c
+ *     = elements [c*L/p, (c+1)*L/p) (integer division);
+ *   - chunk c's running sum starts with rank c's partial and adds ranks c+1,
+ *     c+2, ..., c+p-1 (mod p), one per hop;
+ *   - the bias is added once, after the all-reduce; this oracle returns that
+ *     sum unrounded (fp64).
+ * wire_bf16 != 0 selects the bf16 wire, else fp32.
+ */
+int orc_row_parallel_ring(int tp, int64_t M, int64_t K, int64_t N, const float* X,
+                          int64_t ldx, const float* W, int64_t ldw, const float* b,
+                          int wire_bf16, double* Y, int64_t ldy) {
+  if (tp < 1) return ORC_ERR_BAD_SHAPE;
+  if (M < 0 || K < 0 || N < 0) return ORC_ERR_BAD_SHAPE;
+  if (K % tp != 0) return ORC_ERR_NOT_DIVISIBLE;
+  const int64_t ks = K / tp;
+  const int64_t L = M * N;
+  double* part = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L * tp : 1));
+  if (!part) return ORC_ERR_NOMEM;
+  for (int i = 0; i < tp; ++i) {
+    /* rank i's local partial, held in the wire dtype */
+    double* pi = part + (int64_t)i * L;
+    int rc = orc_linear(M, ks, N, X + (int64_t)i * ks, ldx, W + (int64_t)i * ks, ldw, NULL,
+                        ORC_ACT_NONE, pi, N);
+    if (rc != ORC_OK) {
+      free(part);
+      return rc;
+    }
+    for (int64_t e = 0; e < L; ++e) pi[e] = wire_bf16 ? orc_round_bf16(pi[e]) : orc_round_f32(pi[e]);
+  }
+  for (int c = 0; c < tp; ++c) {
+    const int64_t e0 = (int64_t)c * L / tp, e1 = (int64_t)(c + 1) * L / tp;
+    for (int64_t e = e0; e < e1; ++e) {
+      double acc = part[(int64_t)c * L + e];
+      for (int s = 1; s < tp; ++s) {
+        const int r = (c + s) % tp;
+        acc += part[(int64_t)r * L + e];
+        acc = wire_bf16 ? orc_round_bf16(acc) : orc_round_f32(acc);
+      }
+      const int64_t m = e / N, n = e % N;
+      Y[m * ldy + n] = acc + (b ? (double)b[n] : 0.0);
+    }
+  }
+  free(part);
+  return ORC_OK;
+}
+
 /*
  * FFN block: column-parallel first linear with the nonlinearity applied per
  * shard, then row-parallel second linear whose shard-i input is h_i

@@ -240,6 +240,70 @@ def check_uneven_split(orc):
                           _brute_linear(Xi, Wi, bi))
 
 
+def check_ring_allreduce(orc):
+    """The ring-ordered all-reduce ("Tensor parallel serving", "Communication
+    cost"): values worked out by hand from the algorithm, not from the oracle.
+
+    Case A: tp=3, M=1, K=3, N=5, x = [1,1,1], every W row = [256, 1, 1], so the
+    partials are P0 = 256, P1 = P2 = 1 at every element.  L = 5 splits into
+    chunks [0,1), [1,3), [3,5).  In bf16, 256..512 are spaced by 2 and a tie
+    rounds to the even significand (256, 260):
+      chunk 0 starts at rank 0: 256+1=257 -> 256, +1 -> 256;
+      chunk 1 starts at rank 1: 1+1=2, +256=258;
+      chunk 2 starts at rank 2: 1+256=257 -> 256, +1 -> 256.
+    So y = [256, 258, 258, 256, 256]; an fp32 wire is exact: 258 everywhere.
+    Case B: tp=4, M=2, K=4, N=3, x rows [1,1,1,1], W rows [256,1,1,1]; P0 =
+    256, P1..P3 = 1.  L = 6 splits into [0,1), [1,3), [3,4), [4,6):
+      chunk 0: 256 +1 +1 +1, each 257 -> 256: 256;
+      chunk 1: 1+1=2, +1=3, +256=259 -> 260 (tie between 258 and 260);
+      chunk 2: 1+1=2, +256=258, +1=259 -> 260;
+      chunk 3: 1+256=257 -> 256, +1 -> 256, +1 -> 256.
+    Flattened [256, 260, 260, 260, 256, 256] -> [[256,260,260],[260,256,256]].
+    The bias is added once after the all-reduce.  Case C (below) checks that
+    the partials themselves are held in the wire dtype.
+    """
+    X = np.ones((1, 3), np.float32)
+    W = np.tile(np.array([[256, 1, 1]], np.float32), (5, 1))
+    y = orc.row_parallel_ring(3, X, W, None, "bf16")
+    assert np.array_equal(y, [[256, 258, 258, 256, 256]]), y
+    assert np.array_equal(orc.row_parallel_ring(3, X, W, None, "f32"), np.full((1, 5), 258.0))
+    b = np.array([0.5, -1, 2, 0, 3], np.float32)
+    assert np.array_equal(orc.row_parallel_ring(3, X, W, b, "bf16"),
+                          [[256.5, 257, 260, 256, 259]])
+    X = np.ones((2, 4), np.float32)
+    W = np.tile(np.array([[256, 1, 1, 1]], np.float32), (3, 1))
+    y = orc.row_parallel_ring(4, X, W, None, "bf16")
+    assert np.array_equal(y, [[256, 260, 260], [260, 256, 256]]), y
+    # Case C: a partial that bf16 cannot hold.  tp=2, x = [1,1], W rows
+    # [257, 1]: P0 = 257 is held as 256 (a tie, to the even significand),
+    # P1 = 1.  Both chunks: 256 + 1 = 257 -> 256.  (Unrounded partials would
+    # give 258.)
+    y = orc.row_parallel_ring(2, np.ones((1, 2), np.float32),
+                              np.tile(np.array([[257, 1]], np.float32), (2, 1)), None, "bf16")
+    assert np.array_equal(y, [[256, 256]]), y
+    # small integers: every partial and running sum is exact in bf16, so the
+    # ring equals the plain sum; checked against exact integer brute force
+    rng = _rng(77)
+    for tp in (1, 2, 3, 4):
+        X = _int_mat(rng, (3, 4 * tp), -2, 2)
+        W = _int_mat(rng, (5, 4 * tp), -2, 2)
+        b = _int_mat(rng, (5,), -3, 3)
+        assert np.array_equal(orc.row_parallel_ring(tp, X, W, b, "bf16"), _brute_linear(X, W, b))
+    # fp32 wire: within a few fp32 roundings of the exact sum
+    X = rng.standard_normal((4, 96)).astype(np.float32)
+    W = rng.standard_normal((7, 96)).astype(np.float32)
+    exact = X.astype(np.float64) @ W.astype(np.float64).T
+    y = orc.row_parallel_ring(3, X, W, None, "f32")
+    assert np.max(np.abs(y - exact)) <= 6 * 2.0 ** -24 * np.max(np.abs(exact)) * 3
+    import oracle
+    try:
+        orc.row_parallel_ring(3, np.ones((1, 4), np.float32), np.ones((2, 4), np.float32))
+    except oracle.OracleError as e:
+        assert e.code == 2  # tp must divide in_features
+    else:
+        raise AssertionError("row_parallel_ring accepted tp=3 with K=4")
+
+
 def check_divisibility_errors(orc):
     """tp must divide out_features (column), in_features (row) and the heads."""
     import oracle
@@ -334,6 +398,7 @@ ALL_CHECKS = [
     check_identity_weight,
     check_uneven_split,
     check_divisibility_errors,
+    check_ring_allreduce,
     check_mlp_block,
     check_attention_projections,
 ]

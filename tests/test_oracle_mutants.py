@@ -34,6 +34,12 @@ MUTANTS = [
     ("qkv_kv_group", "(int64_t)H * hd + (int64_t)i * hk * hd,", "(int64_t)H * hd,"),
     ("swiglu_swapped", "Y[m * ldy + n] = orc_silu(g) * u;", "Y[m * ldy + n] = orc_silu(u) * g;"),
     ("h_not_rounded", "if (round_h) h[j] = orc_round_bf16(h[j]);", "(void)round_h;"),
+    ("ring_direction", "const int r = (c + s) % tp;", "const int r = (c + tp - s) % tp;"),
+    ("ring_no_hop_rounding", "acc = wire_bf16 ? orc_round_bf16(acc) : orc_round_f32(acc);", ";"),
+    ("ring_chunk_start_rank0", "double acc = part[(int64_t)c * L + e];", "double acc = part[e];"),
+    ("ring_partial_not_rounded",
+     "for (int64_t e = 0; e < L; ++e) pi[e] = wire_bf16 ? orc_round_bf16(pi[e]) : orc_round_f32(pi[e]);",
+     ";"),
 ]
 
 
