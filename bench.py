@@ -52,6 +52,10 @@ WORKLOADS = {
                                       bias=False),
     "gelu_ffn_tp2": dict(kind="ffn", M=16, d=512, dff=2048, tp=2, act="gelu", bias=True),
     "attn_proj_tp8": dict(kind="attn", M=2048, d=8192, H=64, Hkv=8, hd=128, tp=8),
+    # one decoder layer's linear algebra (QKV, O, FFN up, FFN down) per step,
+    # replayed from a CUDA graph of tp_layer_forward
+    "layer_decode_tp4_b8_graph": dict(kind="layer", M=8, d=8192, H=64, Hkv=8, hd=128,
+                                      dff=28672, tp=4, act="swiglu", bias=False),
 }
 DEFAULT_WORKLOAD = "swiglu_ffn_prefill_tp8"
 
@@ -63,6 +67,12 @@ def kernel_work(w):
     bf16 operands (2 bytes), fp32 biases, bf16 intermediate h, bf16 output.
     """
     M, d = w["M"], w["d"]
+    if w["kind"] == "layer":
+        a = kernel_work(dict(w, kind="attn"))
+        f = kernel_work(dict(w, kind="ffn"))
+        flops = sum(x for x, _ in list(a.values()) + list(f.values()))
+        nbytes = sum(y for _, y in list(a.values()) + list(f.values()))
+        return {"layer": (flops, nbytes)}
     if w["kind"] == "ffn":
         dff = w["dff"]
         n_w1 = 2 if w["act"] == "swiglu" else 1
@@ -272,6 +282,22 @@ class Path:
             self.h = torch.empty(w["M"], w["dff"], dtype=torch.bfloat16, device=device)
             self.Y = torch.empty(w["M"], w["d"], dtype=torch.bfloat16, device=device)
             del f
+        elif w["kind"] == "layer":
+            a = inputs.attn(seed, w["M"], w["d"], w["H"], w["Hkv"], w["hd"], device=device)
+            f = inputs.ffn(seed + 100, w["M"], w["d"], w["dff"], w["act"], w["bias"],
+                           device=device)
+            heads = dict(n_heads=w["H"], n_kv_heads=w["Hkv"], head_dim=w["hd"])
+            wq, _ = tpla.tp_shard_weights("qkv_heads", tp, a.Wqkv, **heads)
+            wo, _ = tpla.tp_shard_weights("row", tp, a.Wo)
+            w1, _ = tpla.tp_shard_weights("gate_up", tp, f.W1, W_up=f.W_up)
+            w2, _ = tpla.tp_shard_weights("row", tp, f.W2)
+            self.X, self.ctx = a.X, a.ctx
+            self.layer_kw = dict(X=a.X, wqkv_shards=wq, bqkv_shards=None, ctx=a.ctx,
+                                 wo_shards=wo, bo=None, w1_shards=w1, b1_shards=None,
+                                 w2_shards=w2, b2=None, ffn_act=w["act"], d_ff=w["dff"], **heads)
+            self.graph = tpla.LayerGraph(tp, **self.layer_kw)
+            self.Y = self.graph.outputs[3]
+            del a, f
         else:
             a = inputs.attn(seed, w["M"], w["d"], w["H"], w["Hkv"], w["hd"], device=device)
             heads = dict(n_heads=w["H"], n_kv_heads=w["Hkv"], head_dim=w["hd"])
@@ -297,6 +323,8 @@ class Path:
             def row(s):
                 t.row_parallel_linear(w["tp"], self.h, self.w2, self.b2, Y=self.Y, stream=s)
             return [("column", column), ("row", row)]
+        if w["kind"] == "layer":
+            return [("layer", lambda s: self.graph.replay())]
         return [("attn_proj", lambda s: self.step_public(s))]
 
     def step_public(self, s, X=None, Y=None):
@@ -304,16 +332,22 @@ class Path:
         w, t = self.w, self.tpla
         X = self.X if X is None else X
         Y = self.Y if Y is None else Y
-        if w["kind"] == "ffn":
+        if w["kind"] == "layer":
+            # the graph reads the captured X buffer and writes the captured output
+            if X is not self.X:
+                self.X.copy_(X, non_blocking=True)
+            self.graph.replay()
+            if Y is not self.Y:
+                Y.copy_(self.Y, non_blocking=True)
+        elif w["kind"] == "ffn":
             t.tp_mlp_block(w["tp"], X, self.w1, self.b1, self.w2, self.b2, w["act"],
                            d_ff=w["dff"], h=self.h, Y=Y, stream=s)
         else:
             t.tp_attn_proj(w["tp"], X, self.w1, None, self.ctx, self.w2, None, w["H"], w["Hkv"],
                            w["hd"], qkv_out=self.qkv, Y=Y, stream=s)
 
-    @staticmethod
-    def launches_per_step():
-        return 2
+    def launches_per_step(self):
+        return 4 if self.w["kind"] == "layer" else 2
 
 
 def run_ours(args, w, rank, local_rank, world):
@@ -383,6 +417,11 @@ def run_ours(args, w, rank, local_rank, world):
         flops, nbytes = work[dom]
         dur_s = avg[dom] / 1e3
         launches_in_dom = 1
+    elif w["kind"] == "layer":
+        dom = "layer"
+        flops, nbytes = work["layer"]
+        dur_s = (sum(per_part["layer"]) / K) / 1e3
+        launches_in_dom = 4
     else:
         dom = "attn_proj"
         flops = sum(f for f, _ in work.values())
@@ -473,6 +512,11 @@ def oracle_inputs(w, rows, seed=20_000):
     a = dict(X=at.X[rows].float().cpu().numpy(), Wqkv=at.Wqkv.float().cpu().numpy(),
              ctx=at.ctx[rows].float().cpu().numpy(), Wo=at.Wo.float().cpu().numpy())
     del at
+    if w["kind"] == "layer":
+        f = inputs.ffn(seed + 100, w["M"], w["d"], w["dff"], w["act"], w["bias"], device=dev)
+        a.update(W1=f.W1.float().cpu().numpy(), W1u=f.W_up.float().cpu().numpy(),
+                 W2=f.W2.float().cpu().numpy())
+        del f
     return a
 
 
@@ -480,9 +524,15 @@ def oracle_step(orc, w, a):
     if w["kind"] == "ffn":
         orc.mlp_block(w["tp"], a["X"], a["W1"], a["b1"], a["W2"], a["b2"], w["act"], W1u=a["W1u"],
                       round_h=True)
-    else:
-        orc.qkv_proj(w["tp"], a["X"], a["Wqkv"], None, w["H"], w["Hkv"], w["hd"])
-        orc.o_proj(w["tp"], a["ctx"], a["Wo"], None, w["H"], w["hd"])
+        return
+    orc.qkv_proj(w["tp"], a["X"], a["Wqkv"], None, w["H"], w["Hkv"], w["hd"])
+    y = orc.o_proj(w["tp"], a["ctx"], a["Wo"], None, w["H"], w["hd"])
+    if w["kind"] == "layer":
+        # the FFN reads the attention block's output, stored in bf16
+        import numpy as np
+        y = np.vectorize(orc.round_bf16)(y)
+        orc.mlp_block(w["tp"], y, a["W1"], None, a["W2"], None, w["act"], W1u=a["W1u"],
+                      round_h=True)
 
 
 def cpu_baseline(w, budget_s=15.0):

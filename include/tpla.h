@@ -213,6 +213,75 @@ tp_status row_parallel_linear(int tp, int64_t M, int64_t K, int64_t N,
                               tp_stream_t stream);
 
 /*
+ * row_parallel_linear_ring -- row_parallel_linear with the shard sum done the
+ * way a ring all-reduce adds the partials on real devices, instead of in one
+ * fp32 accumulator.
+ *
+ * [P5] "Communication cost" (the ring all-reduce: the message is cut into tp
+ * chunks; in the reduce-scatter each chunk's running sum travels once around
+ * the ring, gaining one rank's partial per hop; the all-gather copies the
+ * finished chunks); [P3] RowParallelLinear (all_reduce SUM of each rank's
+ * local partial, then + bias).  Readings where the pages leave the arithmetic
+ * open:
+ *   - rank i's partial X_i . W_i^T is accumulated in fp32 and held in the
+ *     wire dtype (bf16 rounded to nearest even, or fp32);
+ *   - the flattened [M, N] message of L = M*N elements is cut into chunks
+ *     c = [c*L/tp, (c+1)*L/tp) (integer division);
+ *   - chunk c's sum starts with rank c's partial and adds ranks c+1, ...,
+ *     c+tp-1 (mod tp), each addition in fp32 rounded to the wire dtype (every
+ *     hop transmits the running sum in that dtype);
+ *   - the bias is added once, after the all-reduce, in fp32; the result is
+ *     rounded once to ydt.
+ * With a bf16 wire this shows the rounding that a real bf16 all-reduce adds
+ * on top of the fused single-accumulator sum.
+ *
+ *   M, K, N, X, ldx, xdt, w_shards, b, Y, ldy, ydt   as row_parallel_linear.
+ *   wire_dt      TP_BF16 or TP_F32 (TP_F32 needs xdt == TP_F32 or TP_BF16;
+ *                TP_BF16 needs xdt == TP_BF16).
+ *   partials     caller-provided workspace [tp][M][N], contiguous, of dtype
+ *                wire_dt; on return (stream order) it holds the partials.
+ * Launches tp partial GEMMs and one reduction kernel.
+ * Errors: as row_parallel_linear, and TP_ERR_NULL for partials.
+ */
+tp_status row_parallel_linear_ring(int tp, int64_t M, int64_t K, int64_t N,
+                                   const void* X, int64_t ldx, tp_dtype xdt,
+                                   const void* const* w_shards, const float* b,
+                                   tp_dtype wire_dt, void* partials, void* Y,
+                                   int64_t ldy, tp_dtype ydt,
+                                   tp_stream_t stream);
+
+/*
+ * tp_shard_weights_uneven / column_parallel_linear_uneven -- the column split
+ * with explicit per-shard output widths, e.g. 9 outputs as 5 + 4.
+ *
+ * [P5] "Try it yourself" (split 9 output features unevenly, 5 + 4; the
+ * concatenation still equals the full product).  This relaxes the equal-width
+ * assert of [P3]'s ColumnParallelLinear for the column side only.
+ *
+ *   widths       host array of tp widths, each >= 1; sum = out_f (= N).
+ *   Sharding: shard i = rows [w_0 + ... + w_{i-1}, ... + w_i) of W, a
+ *   contiguous [widths[i], in_f] buffer (and fp32 bias slice [widths[i]]).
+ *   Compute: shard i writes columns [w_0 + ... + w_{i-1}, ...) of Y, with
+ *   act TP_ACT_NONE or TP_ACT_GELU_ERF (TP_ACT_SWIGLU: TP_ERR_UNSUPPORTED).
+ *   Each shard runs as a one-shard column call, so the result is bit-identical
+ *   to the same call with tp = 1.
+ *   Other arguments as tp_shard_weights / column_parallel_linear.
+ * Errors: TP_ERR_NULL, TP_ERR_BAD_SHAPE (a width < 1, widths not summing to
+ * out_f), TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_UNSUPPORTED, TP_ERR_CUDA.
+ */
+tp_status tp_shard_weights_uneven(int tp, const int64_t* widths, tp_dtype wdt,
+                                  const void* W, int64_t out_f, int64_t in_f,
+                                  const float* b, void* const* w_shards,
+                                  float* const* b_shards, tp_stream_t stream);
+tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M,
+                                        int64_t K, const void* X, int64_t ldx,
+                                        tp_dtype xdt,
+                                        const void* const* w_shards,
+                                        const float* const* b_shards, tp_act act,
+                                        void* Y, int64_t ldy, tp_dtype ydt,
+                                        tp_stream_t stream);
+
+/*
  * tp_mlp_block -- the tensor-parallel FFN block: column-parallel first linear
  * with the activation applied per shard, then row-parallel second linear whose
  * shard-i input is h_i, summed in the kernel, + b2 once.
@@ -276,6 +345,63 @@ tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads,
                        tp_dtype qkv_dt, const void* ctx,
                        const void* const* wo_shards, const float* bo, void* Y,
                        tp_dtype ydt, tp_stream_t stream);
+
+/*
+ * tp_layer_args / tp_layer_forward -- the linear algebra of one transformer
+ * layer in one call: the attention projections (QKV column-parallel by head
+ * group, O row-parallel by head with the shard sum in the kernel), then the FFN
+ * block (column-parallel with the activation per shard, row-parallel with the
+ * shard sum).  Four launches on one stream, in that order; every argument of
+ * all four is validated before the first one.
+ *
+ * [P4] "How a layer is split" and "Why it helps when serving" (the attention
+ * heads and the FFN are split the same way in every layer; two all-reduces
+ * per layer, one after each block); [P3] "How Tensor Parallelism Works Under
+ * the Hood"; [P5] "Column-parallel and row-parallel layers, paired".
+ *
+ * The steps between the two blocks -- the attention core, residual additions,
+ * normalisation -- are not part of this library, so their results are inputs:
+ * ctx is the attention output, X_ffn the FFN block's input.  X_ffn may be
+ * Y_attn itself (the FFN then reads the attention block's output; Y_attn must
+ * then have dtype xdt).  The call captures into a CUDA graph like any other
+ * sequence of launches (call it once before capturing, so that one-time set-up
+ * happens outside the capture).
+ *
+ * Fields have the meaning, layout and alignment of the same arguments of
+ * tp_attn_proj (tp .. attn_ydt) and tp_mlp_block (d_ff .. ffn_ydt); X and X_ffn
+ * are [M, d_model].  Errors: as tp_attn_proj and tp_mlp_block, and
+ * TP_ERR_NULL for a NULL args pointer.
+ */
+typedef struct {
+  int tp;
+  int64_t M, d_model;
+  tp_dtype xdt;
+  /* attention projections */
+  int n_heads, n_kv_heads, head_dim;
+  const void* X;
+  const void* const* wqkv_shards;
+  const float* const* bqkv_shards;
+  void* qkv_out;
+  tp_dtype qkv_dt;
+  const void* ctx;
+  const void* const* wo_shards;
+  const float* bo;
+  void* Y_attn;
+  tp_dtype attn_ydt;
+  /* FFN block */
+  int64_t d_ff;
+  tp_act ffn_act;
+  const void* X_ffn;
+  const void* const* w1_shards;
+  const float* const* b1_shards;
+  const void* const* w2_shards;
+  const float* b2;
+  void* h;
+  void* Y_ffn;
+  tp_dtype ffn_ydt;
+} tp_layer_args;
+
+tp_status tp_layer_forward(const tp_layer_args* args, tp_stream_t stream);
 
 /*
  * Size in bytes of the workspace built into the library for

@@ -133,6 +133,76 @@ LinearProblem row_problem(int tp, int64_t M, int64_t K, int64_t N, const void* X
   return p;
 }
 
+// Validation and problem set-up of the FFN block, before anything is
+// launched.  *empty: no tokens, nothing to launch.
+tp_status prepare_mlp(int tp, int64_t M, int64_t d_model, int64_t d_ff, int act, int xdt,
+                      const void* X, const void* const* w1_shards, const float* const* b1_shards,
+                      const void* const* w2_shards, const float* b2, void* h, void* Y, int ydt,
+                      LinearProblem* up, LinearProblem* down, bool* empty) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || d_model <= 0 || d_ff <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(d_ff % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(xdt, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(!valid_act(act), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(act == TP_ACT_SWIGLU && b1_shards, TP_ERR_UNSUPPORTED);
+  *empty = (M == 0);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !h || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w1_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_ptr_array(w2_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(b1_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  TP_RET_IF(!al16(X) || !al16(h) || (d_model * es) % 16 || ((d_ff / tp) * es) % 16,
+            TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)) || (b2 && !al_to(b2, 4)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(w1_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_aligned_array(w2_shards, tp)) != TP_OK, st);
+  // h = act(X . W1_i^T + b1_i), shard i in columns [i*d_ff/tp, ...): stored in
+  // the input dtype (bf16 for bf16 inputs).
+  *up = column_problem(tp, M, d_model, d_ff, X, d_model, xdt, w1_shards, b1_shards, act, h, d_ff,
+                       xdt, d_ff / tp);
+  // Y = sum_i h_i . W2_i^T + b2
+  *down = row_problem(tp, M, d_ff, d_model, h, d_ff, xdt, w2_shards, b2, Y, d_model, ydt);
+  return TP_OK;
+}
+
+// Validation and problem set-up of the attention projections.
+tp_status prepare_attn(int tp, int64_t M, int64_t d_model, int n_heads, int n_kv_heads,
+                       int head_dim, int xdt, const void* X, const void* const* wqkv_shards,
+                       const float* const* bqkv_shards, void* qkv_out, int qkv_dt,
+                       const void* ctx, const void* const* wo_shards, const float* bo, void* Y,
+                       int ydt, LinearProblem* qkv, LinearProblem* o, bool* empty) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || d_model <= 0 || n_heads < 1 || n_kv_heads < 1 || head_dim < 1,
+            TP_ERR_BAD_SHAPE);
+  TP_RET_IF(n_heads % tp || n_kv_heads % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(xdt, ydt) || !valid_io(xdt, qkv_dt), TP_ERR_DTYPE);
+  *empty = (M == 0);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !qkv_out || !ctx || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(wqkv_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_ptr_array(wo_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(bqkv_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  const int64_t kq = (int64_t)n_heads * head_dim;        // ctx width
+  const int64_t ks = (int64_t)(n_heads / tp) * head_dim;  // ctx columns per shard
+  const int64_t ws = (int64_t)(n_heads / tp + 2 * (n_kv_heads / tp)) * head_dim;
+  TP_RET_IF(!al16(X) || !al16(ctx) || (d_model * es) % 16 || (kq * es) % 16 || (ks * es) % 16,
+            TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(qkv_out, esz(qkv_dt)) || !al_to(Y, esz(ydt)) || (bo && !al_to(bo, 4)),
+            TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(wqkv_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_aligned_array(wo_shards, tp)) != TP_OK, st);
+  // QKV: shard i -> qkv_out[i] = [M, ws]
+  *qkv = column_problem(tp, M, d_model, ws * tp, X, d_model, xdt, wqkv_shards, bqkv_shards,
+                        TP_ACT_NONE, qkv_out, ws, qkv_dt, M * ws);
+  // O: Y = sum_i ctx_i . Wo_i^T + bo
+  *o = row_problem(tp, M, kq, d_model, ctx, kq, xdt, wo_shards, bo, Y, d_model, ydt);
+  return TP_OK;
+}
+
 }  // namespace
 }  // namespace tpla
 
@@ -276,36 +346,121 @@ tp_status row_parallel_linear(int tp, int64_t M, int64_t K, int64_t N, const voi
   return run(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+tp_status row_parallel_linear_ring(int tp, int64_t M, int64_t K, int64_t N, const void* X,
+                                   int64_t ldx, tp_dtype xdt, const void* const* w_shards,
+                                   const float* b, tp_dtype wire_dt, void* partials, void* Y,
+                                   int64_t ldy, tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || K <= 0 || N <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(K % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(xdt, ydt) || !valid_io(xdt, wire_dt), TP_ERR_DTYPE);
+  TP_RET_IF(ldx < K || ldy < N, TP_ERR_BAD_SHAPE);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !Y || !partials, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  const int64_t ks = K / tp;
+  TP_RET_IF(!al16(X) || (ldx * es) % 16 || (ks * es) % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)) || !al_to(partials, esz(wire_dt)) || (b && !al_to(b, 4)),
+            TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(w_shards, tp)) != TP_OK, st);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // rank i's local partial X_i . W_i^T, rounded once to the wire dtype
+  const int64_t L = M * N;
+  for (int i = 0; i < tp; ++i) {
+    const void* xi = static_cast<const char*>(X) + (int64_t)i * ks * es;
+    void* pi = static_cast<char*>(partials) + (int64_t)i * L * esz(wire_dt);
+    LinearProblem p = row_problem(1, M, ks, N, xi, ldx, xdt, &w_shards[i], nullptr, pi, N,
+                                  wire_dt);
+    if ((st = run(p, s)) != TP_OK) return st;
+  }
+  return launch_ring_reduce(tp, M, N, partials, wire_dt, b, Y, ldy, ydt, s);
+}
+
+tp_status tp_shard_weights_uneven(int tp, const int64_t* widths, tp_dtype wdt, const void* W,
+                                  int64_t out_f, int64_t in_f, const float* b,
+                                  void* const* w_shards, float* const* b_shards,
+                                  tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(!widths, TP_ERR_NULL);
+  TP_RET_IF(!valid_dtype(wdt), TP_ERR_DTYPE);
+  TP_RET_IF(out_f <= 0 || in_f <= 0, TP_ERR_BAD_SHAPE);
+  int64_t total = 0;
+  for (int i = 0; i < tp; ++i) {
+    TP_RET_IF(widths[i] < 1, TP_ERR_BAD_SHAPE);
+    total += widths[i];
+  }
+  TP_RET_IF(total != out_f, TP_ERR_BAD_SHAPE);
+  tp_status st;
+  TP_RET_IF(!W, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w_shards, tp)) != TP_OK, st);
+  if (b) TP_RET_IF((st = check_ptr_array(reinterpret_cast<const void* const*>(b_shards), tp)) != TP_OK, st);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t row_bytes = in_f * esz(wdt);
+  int64_t off = 0;
+  for (int i = 0; i < tp; ++i) {
+    // shard i = rows [off, off + widths[i]) of W: one contiguous block
+    if (cudaMemcpyAsync(w_shards[i], static_cast<const char*>(W) + off * row_bytes,
+                        (size_t)(widths[i] * row_bytes), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return TP_ERR_CUDA;
+    if (b && cudaMemcpyAsync(b_shards[i], b + off, (size_t)widths[i] * sizeof(float),
+                             cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return TP_ERR_CUDA;
+    off += widths[i];
+  }
+  return TP_OK;
+}
+
+tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M, int64_t K,
+                                        const void* X, int64_t ldx, tp_dtype xdt,
+                                        const void* const* w_shards,
+                                        const float* const* b_shards, tp_act act, void* Y,
+                                        int64_t ldy, tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(!widths, TP_ERR_NULL);
+  TP_RET_IF(M < 0 || K <= 0, TP_ERR_BAD_SHAPE);
+  int64_t N = 0;
+  for (int i = 0; i < tp; ++i) {
+    TP_RET_IF(widths[i] < 1, TP_ERR_BAD_SHAPE);
+    N += widths[i];
+  }
+  TP_RET_IF(!valid_io(xdt, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(act != TP_ACT_NONE && act != TP_ACT_GELU_ERF, TP_ERR_UNSUPPORTED);
+  TP_RET_IF(ldx < K || ldy < N, TP_ERR_BAD_SHAPE);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(w_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(b_shards, tp)) != TP_OK, st);
+  const int64_t es = esz(xdt);
+  TP_RET_IF(!al16(X) || (ldx * es) % 16 || (K * es) % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(w_shards, tp)) != TP_OK, st);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int64_t off = 0;
+  for (int i = 0; i < tp; ++i) {
+    // shard i writes columns [off, off + widths[i]) of Y, computed as a
+    // one-shard column call: the same kernel and summation order as tp = 1
+    void* yi = static_cast<char*>(Y) + off * esz(ydt);
+    LinearProblem p = column_problem(1, M, K, widths[i], X, ldx, xdt, &w_shards[i],
+                                     b_shards ? &b_shards[i] : nullptr, act, yi, ldy, ydt, 0);
+    if ((st = run(p, s)) != TP_OK) return st;
+    off += widths[i];
+  }
+  return TP_OK;
+}
+
 tp_status tp_mlp_block(int tp, int64_t M, int64_t d_model, int64_t d_ff, tp_act act, tp_dtype xdt,
                        const void* X, const void* const* w1_shards, const float* const* b1_shards,
                        const void* const* w2_shards, const float* b2, void* h, void* Y,
                        tp_dtype ydt, tp_stream_t stream) {
-  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
-  TP_RET_IF(M < 0 || d_model <= 0 || d_ff <= 0, TP_ERR_BAD_SHAPE);
-  TP_RET_IF(d_ff % tp, TP_ERR_NOT_DIVISIBLE);
-  TP_RET_IF(!valid_io(xdt, ydt), TP_ERR_DTYPE);
-  TP_RET_IF(!valid_act(act), TP_ERR_BAD_SHAPE);
-  TP_RET_IF(act == TP_ACT_SWIGLU && b1_shards, TP_ERR_UNSUPPORTED);
-  if (M == 0) return TP_OK;
-  tp_status st;
-  TP_RET_IF(!X || !h || !Y, TP_ERR_NULL);
-  TP_RET_IF((st = check_ptr_array(w1_shards, tp)) != TP_OK, st);
-  TP_RET_IF((st = check_ptr_array(w2_shards, tp)) != TP_OK, st);
-  TP_RET_IF((st = check_bias_array(b1_shards, tp)) != TP_OK, st);
-  const int64_t es = esz(xdt);
-  TP_RET_IF(!al16(X) || !al16(h) || (d_model * es) % 16 || ((d_ff / tp) * es) % 16,
-            TP_ERR_ALIGNMENT);
-  TP_RET_IF(!al_to(Y, esz(ydt)) || (b2 && !al_to(b2, 4)), TP_ERR_ALIGNMENT);
-  TP_RET_IF((st = check_aligned_array(w1_shards, tp)) != TP_OK, st);
-  TP_RET_IF((st = check_aligned_array(w2_shards, tp)) != TP_OK, st);
+  LinearProblem up, down;
+  bool empty = false;
+  tp_status st = prepare_mlp(tp, M, d_model, d_ff, act, xdt, X, w1_shards, b1_shards, w2_shards,
+                             b2, h, Y, ydt, &up, &down, &empty);
+  if (st != TP_OK || empty) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // h = act(X . W1_i^T + b1_i), shard i in columns [i*d_ff/tp, ...): stored in
-  // the input dtype (bf16 for bf16 inputs).
-  LinearProblem up = column_problem(tp, M, d_model, d_ff, X, d_model, xdt, w1_shards, b1_shards,
-                                    act, h, d_ff, xdt, d_ff / tp);
-  // Y = sum_i h_i . W2_i^T + b2
-  LinearProblem down = row_problem(tp, M, d_ff, d_model, h, d_ff, xdt, w2_shards, b2, Y, d_model,
-                                   ydt);
   if ((st = run(up, s)) != TP_OK) return st;
   return run(down, s);
 }
@@ -315,35 +470,39 @@ tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads, int n_kv
                        const float* const* bqkv_shards, void* qkv_out, tp_dtype qkv_dt,
                        const void* ctx, const void* const* wo_shards, const float* bo, void* Y,
                        tp_dtype ydt, tp_stream_t stream) {
-  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
-  TP_RET_IF(M < 0 || d_model <= 0 || n_heads < 1 || n_kv_heads < 1 || head_dim < 1,
-            TP_ERR_BAD_SHAPE);
-  TP_RET_IF(n_heads % tp || n_kv_heads % tp, TP_ERR_NOT_DIVISIBLE);
-  TP_RET_IF(!valid_io(xdt, ydt) || !valid_io(xdt, qkv_dt), TP_ERR_DTYPE);
-  if (M == 0) return TP_OK;
-  tp_status st;
-  TP_RET_IF(!X || !qkv_out || !ctx || !Y, TP_ERR_NULL);
-  TP_RET_IF((st = check_ptr_array(wqkv_shards, tp)) != TP_OK, st);
-  TP_RET_IF((st = check_ptr_array(wo_shards, tp)) != TP_OK, st);
-  TP_RET_IF((st = check_bias_array(bqkv_shards, tp)) != TP_OK, st);
-  const int64_t es = esz(xdt);
-  const int64_t kq = (int64_t)n_heads * head_dim;        // ctx width
-  const int64_t ks = (int64_t)(n_heads / tp) * head_dim;  // ctx columns per shard
-  const int64_t ws = (int64_t)(n_heads / tp + 2 * (n_kv_heads / tp)) * head_dim;
-  TP_RET_IF(!al16(X) || !al16(ctx) || (d_model * es) % 16 || (kq * es) % 16 || (ks * es) % 16,
-            TP_ERR_ALIGNMENT);
-  TP_RET_IF(!al_to(qkv_out, esz(qkv_dt)) || !al_to(Y, esz(ydt)) || (bo && !al_to(bo, 4)),
-            TP_ERR_ALIGNMENT);
-  TP_RET_IF((st = check_aligned_array(wqkv_shards, tp)) != TP_OK, st);
-  TP_RET_IF((st = check_aligned_array(wo_shards, tp)) != TP_OK, st);
+  LinearProblem qkv, o;
+  bool empty = false;
+  tp_status st = prepare_attn(tp, M, d_model, n_heads, n_kv_heads, head_dim, xdt, X, wqkv_shards,
+                              bqkv_shards, qkv_out, qkv_dt, ctx, wo_shards, bo, Y, ydt, &qkv, &o,
+                              &empty);
+  if (st != TP_OK || empty) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // QKV: shard i -> qkv_out[i] = [M, ws]
-  LinearProblem qkv = column_problem(tp, M, d_model, ws * tp, X, d_model, xdt, wqkv_shards,
-                                     bqkv_shards, TP_ACT_NONE, qkv_out, ws, qkv_dt, M * ws);
-  // O: Y = sum_i ctx_i . Wo_i^T + bo
-  LinearProblem o = row_problem(tp, M, kq, d_model, ctx, kq, xdt, wo_shards, bo, Y, d_model, ydt);
   if ((st = run(qkv, s)) != TP_OK) return st;
   return run(o, s);
+}
+
+tp_status tp_layer_forward(const tp_layer_args* a, tp_stream_t stream) {
+  TP_RET_IF(!a, TP_ERR_NULL);
+  LinearProblem qkv, o, up, down;
+  bool empty_attn = false, empty_mlp = false;
+  tp_status st = prepare_attn(a->tp, a->M, a->d_model, a->n_heads, a->n_kv_heads, a->head_dim,
+                              a->xdt, a->X, a->wqkv_shards, a->bqkv_shards, a->qkv_out, a->qkv_dt,
+                              a->ctx, a->wo_shards, a->bo, a->Y_attn, a->attn_ydt, &qkv, &o,
+                              &empty_attn);
+  if (st != TP_OK) return st;
+  st = prepare_mlp(a->tp, a->M, a->d_model, a->d_ff, a->ffn_act, a->xdt, a->X_ffn, a->w1_shards,
+                   a->b1_shards, a->w2_shards, a->b2, a->h, a->Y_ffn, a->ffn_ydt, &up, &down,
+                   &empty_mlp);
+  if (st != TP_OK) return st;
+  // The FFN may read the attention block's output directly (X_ffn == Y_attn):
+  // then that output must be in the input dtype.
+  TP_RET_IF(a->X_ffn == a->Y_attn && a->attn_ydt != a->xdt, TP_ERR_DTYPE);
+  if (empty_attn) return TP_OK;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = run(qkv, s)) != TP_OK) return st;
+  if ((st = run(o, s)) != TP_OK) return st;
+  if ((st = run(up, s)) != TP_OK) return st;
+  return run(down, s);
 }
 
 tp_status tp_device_status(tp_stream_t stream) {

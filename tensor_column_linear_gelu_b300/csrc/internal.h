@@ -61,6 +61,11 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream);
 bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t ld_bytes, uint32_t box_rows);
 
+// Ring-ordered sum of per-shard partials ([tp][M][N], wire dtype) + bias.
+tp_status launch_ring_reduce(int tp, int64_t M, int64_t N, const void* parts, int wire_dt,
+                             const float* bias, void* Y, int64_t ldy, int ydt,
+                             cudaStream_t stream);
+
 // Shard / pack copies.
 struct ShardJob {
   int split = 0;

@@ -42,8 +42,9 @@ _DT = {torch.float32: TP_F32, torch.bfloat16: TP_BF16}
 
 # Every symbol include/tpla.h declares.
 EXPORTS = ("tp_status_string", "tp_shard_shape", "tp_shard_weights", "column_parallel_linear",
-           "row_parallel_linear", "tp_mlp_block", "tp_attn_proj", "tp_device_status",
-           "tp_selftest_bounded_wait", "tp_mlp_block_noalloc")
+           "row_parallel_linear", "row_parallel_linear_ring", "tp_shard_weights_uneven",
+           "column_parallel_linear_uneven", "tp_mlp_block", "tp_attn_proj", "tp_layer_forward",
+           "tp_device_status", "tp_selftest_bounded_wait", "tp_mlp_block_noalloc")
 
 # ----------------------------------------------------------------- prototypes
 _vp = ctypes.c_void_p
@@ -61,12 +62,32 @@ lib.column_parallel_linear.argtypes = [_int, _i64, _i64, _i64, _vp, _i64, _int, 
                                        _vp, _i64, _int, _vp]
 lib.row_parallel_linear.argtypes = [_int, _i64, _i64, _i64, _vp, _i64, _int, _vpp, _vp, _vp, _i64,
                                     _int, _vp]
+lib.row_parallel_linear_ring.argtypes = [_int, _i64, _i64, _i64, _vp, _i64, _int, _vpp, _vp,
+                                         _int, _vp, _vp, _i64, _int, _vp]
+lib.tp_shard_weights_uneven.argtypes = [_int, _i64p, _int, _vp, _i64, _i64, _vp, _vpp, _vpp, _vp]
+lib.column_parallel_linear_uneven.argtypes = [_int, _i64p, _i64, _i64, _vp, _i64, _int, _vpp,
+                                              _vpp, _int, _vp, _i64, _int, _vp]
 lib.tp_mlp_block.argtypes = [_int, _i64, _i64, _i64, _int, _int, _vp, _vpp, _vpp, _vpp, _vp, _vp,
                              _vp, _int, _vp]
 lib.tp_attn_proj.argtypes = [_int, _i64, _i64, _int, _int, _int, _int, _vp, _vpp, _vpp, _vp, _int,
                              _vp, _vpp, _vp, _vp, _int, _vp]
 lib.tp_mlp_block_noalloc.argtypes = [_int, _i64, _i64, _i64, _int, _int, _vp, _vpp, _vpp, _vpp,
                                      _vp, _vp, _int, _vp]
+
+
+class LayerArgs(ctypes.Structure):
+    """tp_layer_args of include/tpla.h (same field order and C types)."""
+    _fields_ = [("tp", _int), ("M", _i64), ("d_model", _i64), ("xdt", _int),
+                ("n_heads", _int), ("n_kv_heads", _int), ("head_dim", _int),
+                ("X", _vp), ("wqkv_shards", _vpp), ("bqkv_shards", _vpp), ("qkv_out", _vp),
+                ("qkv_dt", _int), ("ctx", _vp), ("wo_shards", _vpp), ("bo", _vp),
+                ("Y_attn", _vp), ("attn_ydt", _int),
+                ("d_ff", _i64), ("ffn_act", _int), ("X_ffn", _vp), ("w1_shards", _vpp),
+                ("b1_shards", _vpp), ("w2_shards", _vpp), ("b2", _vp), ("h", _vp),
+                ("Y_ffn", _vp), ("ffn_ydt", _int)]
+
+
+lib.tp_layer_forward.argtypes = [ctypes.POINTER(LayerArgs), _vp]
 lib.tp_device_status.argtypes = [_vp]
 lib.tp_selftest_bounded_wait.argtypes = [_i64, _vp]
 for _name in EXPORTS[1:]:
@@ -181,6 +202,65 @@ def row_parallel_linear(tp: int, X: torch.Tensor, w_shards, b: Optional[torch.Te
     return Y
 
 
+def row_parallel_linear_ring(tp: int, X: torch.Tensor, w_shards, b: Optional[torch.Tensor] = None,
+                             wire_dtype: torch.dtype = torch.bfloat16,
+                             out_dtype: Optional[torch.dtype] = None,
+                             Y: Optional[torch.Tensor] = None,
+                             partials: Optional[torch.Tensor] = None, stream=None):
+    """Row-parallel linear whose shard sum follows a ring all-reduce: partials
+    held in wire_dtype, chunk c summed from rank c around the ring, rounded to
+    wire_dtype after every hop, + b once.  Returns (Y, partials [tp, M, N])."""
+    M, K = X.shape
+    N = w_shards[0].shape[0]
+    if Y is None:
+        Y = torch.empty(M, N, dtype=out_dtype or X.dtype, device=X.device)
+    if partials is None:
+        partials = torch.empty(tp, M, N, dtype=wire_dtype, device=X.device)
+    _check(lib.row_parallel_linear_ring(tp, M, K, N, ptr(X), X.stride(0), dtype_code(X.dtype),
+                                        ptr_array(w_shards), ptr(b), dtype_code(partials.dtype),
+                                        ptr(partials), ptr(Y), Y.stride(0), dtype_code(Y.dtype),
+                                        stream_handle(stream)),
+           "row_parallel_linear_ring")
+    return Y, partials
+
+
+def _widths(widths):
+    return (ctypes.c_int64 * len(widths))(*[int(w) for w in widths])
+
+
+def tp_shard_weights_uneven(widths: Sequence[int], W: torch.Tensor,
+                            b: Optional[torch.Tensor] = None, stream=None):
+    """Column shards of explicit widths (rows of W).  Returns (w_shards, b_shards or None)."""
+    tp = len(widths)
+    out_f, in_f = W.shape
+    w_sh = [torch.empty(int(w), in_f, dtype=W.dtype, device=W.device) for w in widths]
+    b_sh = None if b is None else [torch.empty(int(w), dtype=torch.float32, device=W.device)
+                                   for w in widths]
+    _check(lib.tp_shard_weights_uneven(tp, _widths(widths), dtype_code(W.dtype), ptr(W), out_f,
+                                       in_f, ptr(b), ptr_array(w_sh), ptr_array(b_sh),
+                                       stream_handle(stream)),
+           "tp_shard_weights_uneven")
+    return w_sh, b_sh
+
+
+def column_parallel_linear_uneven(widths: Sequence[int], X: torch.Tensor, w_shards,
+                                  b_shards=None, act="none",
+                                  out_dtype: Optional[torch.dtype] = None,
+                                  Y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Column split with explicit widths; shard i writes its column block of Y."""
+    M, K = X.shape
+    N = int(sum(widths))
+    if Y is None:
+        Y = torch.empty(M, N, dtype=out_dtype or X.dtype, device=X.device)
+    _check(lib.column_parallel_linear_uneven(len(widths), _widths(widths), M, K, ptr(X),
+                                             X.stride(0), dtype_code(X.dtype),
+                                             ptr_array(w_shards), ptr_array(b_shards), _act(act),
+                                             ptr(Y), Y.stride(0), dtype_code(Y.dtype),
+                                             stream_handle(stream)),
+           "column_parallel_linear_uneven")
+    return Y
+
+
 def tp_mlp_block(tp: int, X: torch.Tensor, w1_shards, b1_shards, w2_shards,
                  b2: Optional[torch.Tensor], act="gelu", d_ff: Optional[int] = None,
                  out_dtype: Optional[torch.dtype] = None, h: Optional[torch.Tensor] = None,
@@ -238,6 +318,74 @@ def tp_mlp_block_noalloc(tp: int, X: torch.Tensor, w1_shards, b1_shards, w2_shar
                                     stream_handle(stream)),
            "tp_mlp_block_noalloc")
     return Y
+
+
+def tp_layer_forward(tp: int, X: torch.Tensor, wqkv_shards, bqkv_shards, ctx: torch.Tensor,
+                     wo_shards, bo: Optional[torch.Tensor], n_heads: int, n_kv_heads: int,
+                     head_dim: int, w1_shards, b1_shards, w2_shards, b2: Optional[torch.Tensor],
+                     ffn_act="swiglu", d_ff: Optional[int] = None, X_ffn="attn",
+                     qkv_out: Optional[torch.Tensor] = None, Y_attn: Optional[torch.Tensor] = None,
+                     h: Optional[torch.Tensor] = None, Y_ffn: Optional[torch.Tensor] = None,
+                     out_dtype: Optional[torch.dtype] = None, qkv_dtype: Optional[torch.dtype] = None,
+                     stream=None):
+    """One layer's linear algebra: QKV and O projections, then the FFN block.
+
+    X_ffn is the FFN block's input; "attn" (the default) feeds it the attention
+    block's output Y_attn, which is then kept in X's dtype.  Returns
+    (qkv_out, Y_attn, h, Y_ffn)."""
+    M, d_model = X.shape
+    if d_ff is None:
+        d_ff = w2_shards[0].shape[1] * tp
+    ws = (n_heads // tp + 2 * (n_kv_heads // tp)) * head_dim if tp > 0 else 0
+    if qkv_out is None:
+        qkv_out = torch.empty(tp, M, ws, dtype=qkv_dtype or X.dtype, device=X.device)
+    feed = isinstance(X_ffn, str) and X_ffn == "attn"
+    if Y_attn is None:
+        Y_attn = torch.empty(M, d_model, dtype=X.dtype if feed else (out_dtype or X.dtype),
+                             device=X.device)
+    if feed:
+        X_ffn = Y_attn
+    if h is None:
+        h = torch.empty(M, d_ff, dtype=X.dtype, device=X.device)
+    if Y_ffn is None:
+        Y_ffn = torch.empty(M, d_model, dtype=out_dtype or X.dtype, device=X.device)
+    keep = [ptr_array(wqkv_shards), ptr_array(bqkv_shards), ptr_array(wo_shards),
+            ptr_array(w1_shards), ptr_array(b1_shards), ptr_array(w2_shards)]
+    a = LayerArgs(tp, M, d_model, dtype_code(X.dtype), n_heads, n_kv_heads, head_dim,
+                  ptr(X), keep[0], keep[1], ptr(qkv_out), dtype_code(qkv_out.dtype), ptr(ctx),
+                  keep[2], ptr(bo), ptr(Y_attn), dtype_code(Y_attn.dtype),
+                  d_ff, _act(ffn_act), ptr(X_ffn), keep[3], keep[4], keep[5], ptr(b2), ptr(h),
+                  ptr(Y_ffn), dtype_code(Y_ffn.dtype))
+    _check(lib.tp_layer_forward(ctypes.byref(a), stream_handle(stream)), "tp_layer_forward")
+    return qkv_out, Y_attn, h, Y_ffn
+
+
+class LayerGraph:
+    """One tp_layer_forward call captured in a CUDA graph.
+
+    The call runs once outside the capture (one-time set-up), then once under
+    torch.cuda.graph; replay() re-runs the four launches with no host work
+    between them.  Inputs are read from, and outputs written to, the tensors
+    given at construction: copy new inputs into them before a replay."""
+
+    def __init__(self, tp: int, **kw):
+        self.tp, self.kw = tp, kw
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.outputs = tp_layer_forward(tp, **kw, stream=side)
+        torch.cuda.current_stream().wait_stream(side)
+        qkv, ya, h, yf = self.outputs
+        kw = dict(kw, qkv_out=qkv, Y_attn=ya, h=h, Y_ffn=yf)
+        if isinstance(kw.get("X_ffn", "attn"), str):
+            kw["X_ffn"] = "attn"
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            tp_layer_forward(tp, **kw)
+
+    def replay(self):
+        self.graph.replay()
+        return self.outputs
 
 
 def tp_device_status(stream=None) -> int:

@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("tp_shard_weights", "column_parallel_linear", "row_parallel_linear",
-                 "tp_mlp_block", "tp_attn_proj", "tp_status_string"):
+                 "tp_mlp_block", "tp_attn_proj", "tp_layer_forward", "tp_status_string"):
         assert must in names
 
 
@@ -123,6 +123,40 @@ rec("shard_notdiv", S(0, 3, BF, A, None, 64, 64, None, 0, 0, 0, arr(A, A, A), No
 rec("shard_row_cols_misaligned", S(1, 2, BF, A, None, 64, 40, None, 0, 0, 0, w2, None, None))
 rec("shard_dtype", S(0, 2, 5, A, None, 64, 64, None, 0, 0, 0, w2, None, None))
 rec("selftest_bad_limit", L.tp_selftest_bounded_wait(0, None))
+# tp_layer_forward(args, s): validation of both blocks before any launch
+rec("layer_null_args", L.tp_layer_forward(None, None))
+def layer(**over):
+    f = dict(tp=2, M=4, d_model=64, xdt=BF, n_heads=4, n_kv_heads=2, head_dim=8, X=A,
+             wqkv_shards=w2, bqkv_shards=None, qkv_out=A, qkv_dt=BF, ctx=A, wo_shards=w2, bo=None,
+             Y_attn=A + 0x100, attn_ydt=BF, d_ff=128, ffn_act=2, X_ffn=A + 0x100, w1_shards=w2,
+             b1_shards=None, w2_shards=w2, b2=None, h=A, Y_ffn=A, ffn_ydt=BF)
+    f.update(over)
+    a = t.LayerArgs(**f)
+    return L.tp_layer_forward(ctypes.byref(a), None)
+rec("layer_M0", layer(M=0, X=None, qkv_out=None, ctx=None, Y_attn=None, X_ffn=None, h=None, Y_ffn=None))
+rec("layer_ffn_notdiv", layer(d_ff=129))
+rec("layer_ffn_null_h", layer(h=None))
+rec("layer_attn_kv_notdiv", layer(n_kv_heads=1))
+rec("layer_feed_dtype", layer(attn_ydt=F32))
+rec("layer_swiglu_bias", layer(b1_shards=w2))
+# row_parallel_linear_ring(tp, M, K, N, X, ldx, xdt, w, b, wire, partials, Y, ldy, ydt, s)
+RR = L.row_parallel_linear_ring
+rec("ring_null_partials", RR(2, 4, 64, 64, A, 64, BF, w2, None, BF, None, A, 64, BF, None))
+rec("ring_wire_bf16_from_f32", RR(2, 4, 64, 64, A, 64, F32, w2, None, BF, A, A, 64, F32, None))
+rec("ring_notdiv", RR(3, 4, 64, 64, A, 64, BF, arr(A, A, A), None, BF, A, A, 64, BF, None))
+rec("ring_M0", RR(2, 0, 64, 64, None, 64, BF, None, None, BF, None, None, 64, BF, None))
+rec("ring_bad_wire", RR(2, 4, 64, 64, A, 64, BF, w2, None, 9, A, A, 64, BF, None))
+# uneven split
+W64 = lambda *v: ctypes.cast((ctypes.c_int64 * len(v))(*v), t._i64p)
+US = L.tp_shard_weights_uneven
+rec("uneven_shard_sum", US(2, W64(5, 3), BF, A, 9, 64, None, w2, None, None))
+rec("uneven_shard_zero", US(2, W64(9, 0), BF, A, 9, 64, None, w2, None, None))
+rec("uneven_shard_null_widths", US(2, None, BF, A, 9, 64, None, w2, None, None))
+UC = L.column_parallel_linear_uneven
+rec("uneven_col_swiglu", UC(2, W64(5, 4), 4, 64, A, 64, BF, w2, None, 2, A, 9, BF, None))
+rec("uneven_col_ldy", UC(2, W64(5, 4), 4, 64, A, 64, BF, w2, None, 0, A, 8, BF, None))
+rec("uneven_col_M0", UC(2, W64(5, 4), 0, 64, None, 64, BF, None, None, 0, None, 9, BF, None))
+rec("uneven_col_width0", UC(2, W64(9, 0), 4, 64, A, 64, BF, w2, None, 0, A, 9, BF, None))
 json.dump(res, sys.stdout)
 '''
 
@@ -138,7 +172,12 @@ EXPECT = {
     "attn_kv_notdiv": 2, "attn_hd0": 3, "attn_null_ctx": 1, "attn_qkv_dtype": 4,
     "shard_row_bias": 8, "shard_gateup_no_up": 1, "shard_bias_no_dst": 1, "shard_null_W": 1,
     "shard_notdiv": 2, "shard_row_cols_misaligned": 5, "shard_dtype": 4,
-    "selftest_bad_limit": 3,
+    "selftest_bad_limit": 3, "layer_null_args": 1, "layer_M0": 0, "layer_ffn_notdiv": 2,
+    "layer_ffn_null_h": 1, "layer_attn_kv_notdiv": 2, "layer_feed_dtype": 4,
+    "layer_swiglu_bias": 8, "ring_null_partials": 1, "ring_wire_bf16_from_f32": 4,
+    "ring_notdiv": 2, "ring_M0": 0, "ring_bad_wire": 4, "uneven_shard_sum": 3,
+    "uneven_shard_zero": 3, "uneven_shard_null_widths": 1, "uneven_col_swiglu": 8,
+    "uneven_col_ldy": 3, "uneven_col_M0": 0, "uneven_col_width0": 3,
 }
 
 
