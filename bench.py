@@ -56,7 +56,27 @@ WORKLOADS = {
     # replayed from a CUDA graph of tp_layer_forward
     "layer_decode_tp4_b8_graph": dict(kind="layer", M=8, d=8192, H=64, Hkv=8, hd=128,
                                       dff=28672, tp=4, act="swiglu", bias=False),
+    # the FFN down projection of the 4096-token prefill, its shard sum done the
+    # way a ring all-reduce adds bf16 partials (tp partial GEMMs + ring kernel)
+    "row_ring_prefill_tp8": dict(kind="row_ring", M=4096, d=8192, dff=28672, tp=8),
+    # d_ff = 28672 is not divisible by 3: tp=3 needs the uneven column split
+    # (up projection of the decode FFN, 8 tokens, widths 9558/9557/9557)
+    "column_uneven_decode_tp3_b8": dict(kind="uneven", M=8, d=8192, dff=28672, tp=3,
+                                        widths=(9558, 9557, 9557)),
 }
+
+# Link bandwidth for the analytic ring all-reduce time of "Tensor parallel
+# serving" ("Communication cost"): T = 2 (p - 1) / p * bytes / B.  A stated
+# assumption (an NVLink-class per-GPU link), not a measurement: no bytes leave
+# the one GPU here.
+LINK_GBPS = 900.0
+
+
+def ring_allreduce_us(p: int, nbytes: float, link_gbps: float = LINK_GBPS) -> float:
+    """Time of a ring all-reduce of nbytes over p ranks at link_gbps, in us."""
+    if p <= 1:
+        return 0.0
+    return 2.0 * (p - 1) / p * nbytes / (link_gbps * 1e9) * 1e6
 DEFAULT_WORKLOAD = "swiglu_ffn_prefill_tp8"
 
 
@@ -67,6 +87,14 @@ def kernel_work(w):
     bf16 operands (2 bytes), fp32 biases, bf16 intermediate h, bf16 output.
     """
     M, d = w["M"], w["d"]
+    if w["kind"] == "row_ring":
+        dff, tp = w["dff"], w["tp"]
+        # partial GEMMs: weights + h + bf16 partials; ring kernel: partials + Y
+        flops = 2.0 * M * dff * d
+        nbytes = 2.0 * (d * dff + M * dff + tp * M * d) + 2.0 * (tp * M * d + M * d)
+        return {"row_ring": (flops, nbytes)}
+    if w["kind"] == "uneven":
+        return {"column": (2.0 * M * d * w["dff"], 2.0 * (w["dff"] * d + M * d + M * w["dff"]))}
     if w["kind"] == "layer":
         a = kernel_work(dict(w, kind="attn"))
         f = kernel_work(dict(w, kind="ffn"))
@@ -282,6 +310,21 @@ class Path:
             self.h = torch.empty(w["M"], w["dff"], dtype=torch.bfloat16, device=device)
             self.Y = torch.empty(w["M"], w["d"], dtype=torch.bfloat16, device=device)
             del f
+        elif w["kind"] == "row_ring":
+            self.h = inputs.normal((w["M"], w["dff"]), 1.0, seed, torch.bfloat16, device)
+            W2 = inputs.normal((w["d"], w["dff"]), inputs.WEIGHT_STD, seed + 3, torch.bfloat16,
+                               device)
+            self.w2, _ = tpla.tp_shard_weights("row", tp, W2)
+            del W2
+            self.X = self.h
+            self.parts_buf = torch.empty(tp, w["M"], w["d"], dtype=torch.bfloat16, device=device)
+            self.Y = torch.empty(w["M"], w["d"], dtype=torch.bfloat16, device=device)
+        elif w["kind"] == "uneven":
+            f = inputs.ffn(seed, w["M"], w["d"], w["dff"], "gelu", False, device=device)
+            self.w1, _ = tpla.tp_shard_weights_uneven(w["widths"], f.W1)
+            self.X = f.X
+            self.Y = torch.empty(w["M"], w["dff"], dtype=torch.bfloat16, device=device)
+            del f
         elif w["kind"] == "layer":
             a = inputs.attn(seed, w["M"], w["d"], w["H"], w["Hkv"], w["hd"], device=device)
             f = inputs.ffn(seed + 100, w["M"], w["d"], w["dff"], w["act"], w["bias"],
@@ -325,14 +368,23 @@ class Path:
             return [("column", column), ("row", row)]
         if w["kind"] == "layer":
             return [("layer", lambda s: self.graph.replay())]
+        if w["kind"] in ("row_ring", "uneven"):
+            return [(w["kind"] if w["kind"] == "row_ring" else "column",
+                     lambda s: self.step_public(s))]
         return [("attn_proj", lambda s: self.step_public(s))]
 
     def step_public(self, s, X=None, Y=None):
         """One step through the public call a user makes."""
+        import torch
         w, t = self.w, self.tpla
         X = self.X if X is None else X
         Y = self.Y if Y is None else Y
-        if w["kind"] == "layer":
+        if w["kind"] == "row_ring":
+            t.row_parallel_linear_ring(w["tp"], X, self.w2, None, wire_dtype=torch.bfloat16,
+                                       Y=Y, partials=self.parts_buf, stream=s)
+        elif w["kind"] == "uneven":
+            t.column_parallel_linear_uneven(w["widths"], X, self.w1, None, "none", Y=Y, stream=s)
+        elif w["kind"] == "layer":
             # the graph reads the captured X buffer and writes the captured output
             if X is not self.X:
                 self.X.copy_(X, non_blocking=True)
@@ -347,7 +399,8 @@ class Path:
                            w["hd"], qkv_out=self.qkv, Y=Y, stream=s)
 
     def launches_per_step(self):
-        return 4 if self.w["kind"] == "layer" else 2
+        return {"layer": 4, "row_ring": self.w["tp"] + 1,
+                "uneven": self.w["tp"]}.get(self.w["kind"], 2)
 
 
 def run_ours(args, w, rank, local_rank, world):
@@ -417,11 +470,11 @@ def run_ours(args, w, rank, local_rank, world):
         flops, nbytes = work[dom]
         dur_s = avg[dom] / 1e3
         launches_in_dom = 1
-    elif w["kind"] == "layer":
-        dom = "layer"
-        flops, nbytes = work["layer"]
-        dur_s = (sum(per_part["layer"]) / K) / 1e3
-        launches_in_dom = 4
+    elif w["kind"] in ("layer", "row_ring", "uneven"):
+        dom = next(iter(work))
+        flops, nbytes = work[dom]
+        dur_s = (sum(per_part[dom]) / K) / 1e3
+        launches_in_dom = path.launches_per_step()
     else:
         dom = "attn_proj"
         flops = sum(f for f, _ in work.values())
@@ -499,6 +552,17 @@ def oracle_inputs(w, rows, seed=20_000):
     import torch
     from tensor_column_linear_gelu_b300 import inputs
     dev = "cuda" if torch.cuda.is_available() else None
+    if w["kind"] == "row_ring":
+        h = inputs.normal((w["M"], w["dff"]), 1.0, seed, torch.bfloat16, dev)
+        W2 = inputs.normal((w["d"], w["dff"]), inputs.WEIGHT_STD, seed + 3, torch.bfloat16, dev)
+        a = dict(X=h[rows].float().cpu().numpy(), W2=W2.float().cpu().numpy())
+        del h, W2
+        return a
+    if w["kind"] == "uneven":
+        f = inputs.ffn(seed, w["M"], w["d"], w["dff"], "gelu", False, device=dev)
+        a = dict(X=f.X[rows].float().cpu().numpy(), W1=f.W1.float().cpu().numpy())
+        del f
+        return a
     if w["kind"] == "ffn":
         f = inputs.ffn(seed, w["M"], w["d"], w["dff"], w["act"], w["bias"], device=dev)
         a = dict(X=f.X[rows].float().cpu().numpy(), W1=f.W1.float().cpu().numpy(),
@@ -521,6 +585,12 @@ def oracle_inputs(w, rows, seed=20_000):
 
 
 def oracle_step(orc, w, a):
+    if w["kind"] == "row_ring":
+        orc.row_parallel_ring(w["tp"], a["X"], a["W2"], None, "bf16")
+        return
+    if w["kind"] == "uneven":
+        orc.column_parallel_uneven(list(w["widths"]), a["X"], a["W1"])
+        return
     if w["kind"] == "ffn":
         orc.mlp_block(w["tp"], a["X"], a["W1"], a["b1"], a["W2"], a["b2"], w["act"], W1u=a["W1u"],
                       round_h=True)
@@ -641,6 +711,14 @@ def main():
             "gpu_launches": r["launches"], "clocks": r["clocks"],
             "kernel_ms": r["per_part"],
         }
+        n_ar = {"ffn": 1, "attn": 1, "layer": 2, "row_ring": 1}.get(w["kind"], 0)
+        if n_ar:
+            msg = 2.0 * w["M"] * w["d"]  # one bf16 [M, d_model] message per all-reduce
+            line["comm_model"] = {
+                "ring_allreduce_us_per_step": round(n_ar * ring_allreduce_us(w["tp"], msg), 3),
+                "allreduces_per_step": n_ar, "bytes_per_allreduce": msg,
+                "link_GBps": LINK_GBPS,
+                "note": "analytic 2(p-1)/p*bytes/B for tp devices; nothing is sent here"}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -105,7 +105,11 @@ LinearProblem column_problem(int tp, int64_t M, int64_t K, int64_t N, const void
   for (int i = 0; i < tp; ++i) {
     p.W[i] = w[i];
     p.bias[i] = b ? b[i] : nullptr;
+    p.fo[i] = (int64_t)i * p.ns;
+    p.wr[i] = p.w_rows;
+    p.yoff[i] = (int64_t)i * y_shard_stride;
   }
+  p.fo[tp] = (int64_t)tp * p.ns;
   return p;
 }
 
@@ -438,10 +442,29 @@ tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M
   TP_RET_IF(!al_to(Y, esz(ydt)), TP_ERR_ALIGNMENT);
   TP_RET_IF((st = check_aligned_array(w_shards, tp)) != TP_OK, st);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (xdt == TP_F32 || M <= kSkinnyMaxTokens) {
+    // one launch over all shards: shard i owns output features [off_i,
+    // off_i + widths[i]) and writes them to the same columns of Y
+    LinearProblem p = column_problem(1, M, K, N, X, ldx, xdt, w_shards, nullptr, act, Y, ldy,
+                                     ydt, 0);
+    p.tp = tp;
+    p.uneven = true;
+    int64_t off = 0;
+    for (int i = 0; i < tp; ++i) {
+      p.W[i] = w_shards[i];
+      p.bias[i] = b_shards ? b_shards[i] : nullptr;
+      p.fo[i] = off;
+      p.wr[i] = widths[i];
+      p.yoff[i] = off;
+      off += widths[i];
+    }
+    p.fo[tp] = off;
+    return run(p, s);
+  }
   int64_t off = 0;
   for (int i = 0; i < tp; ++i) {
-    // shard i writes columns [off, off + widths[i]) of Y, computed as a
-    // one-shard column call: the same kernel and summation order as tp = 1
+    // many tokens: shard i as a one-shard call writing columns [off, off +
+    // widths[i]) of Y -- the prefill GEMM's tiles need an equal split
     void* yi = static_cast<char*>(Y) + off * esz(ydt);
     LinearProblem p = column_problem(1, M, K, widths[i], X, ldx, xdt, &w_shards[i],
                                      b_shards ? &b_shards[i] : nullptr, act, yi, ldy, ydt, 0);

@@ -37,7 +37,9 @@ struct GemvParams {
   int tp;
   int act;
   int ydt;
-  int64_t M, K, n_out, ns, ldx, x_shard_off, ldy, y_shard_stride;
+  int64_t M, K, n_out, ns, ldx, x_shard_off, ldy;
+  int64_t fo[TP_MAX_TP + 1];  // column: shard i owns outputs [fo[i], fo[i+1])
+  int64_t yoff[TP_MAX_TP];    // column: element offset of shard i's outputs in Y
   const void* X;
   const void* W[TP_MAX_TP];
   const float* bias[TP_MAX_TP];
@@ -137,8 +139,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const int64_t o = min(t * R + r, p.n_out - 1);
-          const int64_t i = o / p.ns;
-          const int64_t n = o - i * p.ns;
+          int i = 0;
+          while (i + 1 < p.tp && p.fo[i + 1] <= o) ++i;
+          const int64_t n = o - p.fo[i];
           const T* Wi = reinterpret_cast<const T*>(p.W[i]);
           if constexpr (SW) {
             const int64_t grp = n / G;
@@ -182,15 +185,16 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
             if (p.bias[0]) z += p.bias[0][o];
             store_out(p.Y, p.ydt, m * p.ldy + o, z);
           } else {
-            const int64_t i = o / p.ns;
-            const int64_t n = o - i * p.ns;
+            int i = 0;
+            while (i + 1 < p.tp && p.fo[i + 1] <= o) ++i;
+            const int64_t n = o - p.fo[i];
             if constexpr (SW) {
               z = act_silu(z) * acc[mm][R + r];
             } else {
               if (p.bias[i]) z += p.bias[i][n];
               if constexpr (ACT == TP_ACT_GELU_ERF) z = act_gelu_erf(z);
             }
-            store_out(p.Y, p.ydt, i * p.y_shard_stride + m * p.ldy + n, z);
+            store_out(p.Y, p.ydt, p.yoff[i] + m * p.ldy + n, z);
           }
         }
     }
@@ -253,7 +257,8 @@ tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream) {
   gp.ldx = p.ldx;
   gp.x_shard_off = p.x_shard_off;
   gp.ldy = p.ldy;
-  gp.y_shard_stride = p.y_shard_stride;
+  for (int i = 0; i <= p.tp; ++i) gp.fo[i] = p.fo[i];
+  for (int i = 0; i < p.tp; ++i) gp.yoff[i] = p.yoff[i];
   gp.X = p.X;
   gp.Y = p.Y;
   for (int i = 0; i < TP_MAX_TP; ++i) {

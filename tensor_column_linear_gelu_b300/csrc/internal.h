@@ -39,6 +39,16 @@ struct LinearProblem {
   void* Y = nullptr;
   int64_t ldy = 0;
   int64_t y_shard_stride = 0;  // column: element offset of shard i's output
+  // Column side, shard by shard: output features [fo[i], fo[i+1]) belong to
+  // shard i, whose buffer has wr[i] rows and whose outputs start at element
+  // yoff[i] of Y.  Equal split: fo[i] = i*ns, wr[i] = w_rows,
+  // yoff[i] = i*y_shard_stride.  The decode kernel and the GEMV read these
+  // tables (so they also run uneven splits); the prefill GEMM needs the
+  // equal split.
+  int64_t fo[TP_MAX_TP + 1] = {};
+  int64_t wr[TP_MAX_TP] = {};
+  int64_t yoff[TP_MAX_TP] = {};
+  bool uneven = false;
 };
 
 // Weight-streaming GEMV on CUDA cores (few tokens; also the fp32 path).

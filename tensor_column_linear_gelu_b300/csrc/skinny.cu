@@ -105,8 +105,10 @@ struct SkinnyParams {
   const float* bias[TP_MAX_TP];
   void* Y;
   unsigned int* err;
-  int64_t ldy, y_shard_stride;
-  int64_t M, ns, feat_total;     // feat_total: column tp*ns; row n_out
+  int64_t ldy;
+  int64_t fo[TP_MAX_TP + 1];     // column: shard i owns features [fo[i], fo[i+1])
+  int64_t yoff[TP_MAX_TP];       // column: element offset of shard i's outputs in Y
+  int64_t M, feat_total;         // feat_total: column fo[tp]; row n_out
   int tp, row, act, ydt;
   int xrows, x_stage_bytes, stages;
   int w_stage_bytes;             // weight rows of a B tile x 128 bytes
@@ -176,9 +178,10 @@ __device__ __forceinline__ Tile column_tile(const SkinnyParams& p, int64_t& f, i
   t.kb1 = p.kb_total;
   t.boxes = 0;
   while (f < f1 && t.n < SK_MAX_PIECES && t.rows < cap) {
-    const int64_t sh = f / p.ns;
-    const int64_t loc = f - sh * p.ns;
-    int64_t lim = imin(f1 - f, p.ns - loc);
+    int sh = 0;
+    while (sh + 1 < p.tp && p.fo[sh + 1] <= f) ++sh;
+    const int64_t loc = f - p.fo[sh];
+    int64_t lim = imin(f1 - f, p.fo[sh + 1] - f);
     if (swiglu) lim = imin(lim, G - loc % G);
     const int c = (int)imin(lim, cap - t.rows);
     const int nb = piece_boxes(c) * (swiglu ? 2 : 1);
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         } else if (has_tokens) {
           for (int i = 0; i < tl.n; ++i) {
             const Piece& pc = tl.pc[i];
-            const int64_t base = (p.row ? 0 : (int64_t)pc.shard * p.y_shard_stride) + t * p.ldy;
+            const int64_t base = (p.row ? 0 : p.yoff[pc.shard]) + t * p.ldy;
             const float* bias = p.row ? p.bias[0] : (swiglu ? nullptr : p.bias[pc.shard]);
 #pragma unroll 1
             for (int j0 = 0; j0 < pc.c; j0 += 8) {
@@ -543,19 +546,18 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
     return TP_ERR_CUDA;
   }
   for (int i = 0; i < p.tp; ++i) {
-    if (!make_tma_map_bf16(&sp.tmW16[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows,
-                           (uint64_t)(p.K * es), 16) ||
-        !make_tma_map_bf16(&sp.tmW64[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows,
-                           (uint64_t)(p.K * es), 64))
+    const uint64_t rows = (uint64_t)(p.row ? p.w_rows : p.wr[i]);
+    if (!make_tma_map_bf16(&sp.tmW16[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 16) ||
+        !make_tma_map_bf16(&sp.tmW64[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 64))
       return TP_ERR_CUDA;
   }
   for (int i = 0; i < TP_MAX_TP; ++i) sp.bias[i] = p.bias[i];
   sp.Y = p.Y;
   sp.ldy = p.ldy;
-  sp.y_shard_stride = p.y_shard_stride;
+  for (int i = 0; i <= p.tp; ++i) sp.fo[i] = p.fo[i];
+  for (int i = 0; i < p.tp; ++i) sp.yoff[i] = p.yoff[i];
   sp.M = p.M;
-  sp.ns = p.ns;
-  sp.feat_total = p.row ? p.n_out : (int64_t)p.tp * p.ns;
+  sp.feat_total = p.row ? p.n_out : p.fo[p.tp];
   sp.tp = p.tp;
   sp.row = p.row ? 1 : 0;
   sp.act = p.act;

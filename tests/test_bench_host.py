@@ -1,0 +1,36 @@
+"""Host-side logic of bench.py (CPU only): the work model and the analytic
+ring all-reduce time of "Tensor parallel serving" ("Communication cost")."""
+import math
+
+import bench
+
+
+def test_ring_allreduce_time_model():
+    B = bench.LINK_GBPS * 1e9
+    assert bench.ring_allreduce_us(1, 1e9) == 0.0
+    # p = 2: each rank sends and receives half the message twice -> bytes / B
+    assert math.isclose(bench.ring_allreduce_us(2, 1e9), 1e9 / B * 1e6)
+    # p = 8: 2 * 7/8 = 1.75 message lengths over the link
+    assert math.isclose(bench.ring_allreduce_us(8, 4096 * 8192 * 2), 1.75 * 4096 * 8192 * 2 / B * 1e6)
+    # grows towards 2 * bytes / B as p grows
+    assert bench.ring_allreduce_us(1024, 1e9) < 2 * 1e9 / B * 1e6
+
+
+def test_work_model_covers_every_workload():
+    for name, w in bench.WORKLOADS.items():
+        work = bench.kernel_work(w)
+        assert work, name
+        for flops, nbytes in work.values():
+            assert flops > 0 and nbytes > 0, name
+    # the prefill FFN: 2*M*d*(2 d_ff) for gate+up, 2*M*d_ff*d for down
+    w = bench.WORKLOADS["swiglu_ffn_prefill_tp8"]
+    work = bench.kernel_work(w)
+    assert work["column"][0] == 2.0 * 4096 * 8192 * 2 * 28672
+    assert work["row"][0] == 2.0 * 4096 * 28672 * 8192
+    # decode: weight bytes dominate
+    w = bench.WORKLOADS["swiglu_ffn_decode_tp4_b1"]
+    col, row = bench.kernel_work(w)["column"], bench.kernel_work(w)["row"]
+    assert abs(col[1] - 2 * 2 * 28672 * 8192) < 1e6 and abs(row[1] - 2 * 28672 * 8192) < 1e6
+    # the uneven split's widths cover d_ff
+    w = bench.WORKLOADS["column_uneven_decode_tp3_b8"]
+    assert sum(w["widths"]) == w["dff"] and len(w["widths"]) == w["tp"]
