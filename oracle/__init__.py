@@ -62,7 +62,7 @@ _i64 = ctypes.c_int64
 
 
 def _bind(lib):
-    for name in ("orc_gelu", "orc_silu", "orc_round_bf16", "orc_round_f32"):
+    for name in ("orc_gelu", "orc_silu", "orc_round_bf16", "orc_round_f32", "orc_round_e4m3"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_double
         fn.argtypes = [ctypes.c_double]
@@ -79,6 +79,11 @@ def _bind(lib):
                                      _i64, _f, _d, _i64]
     lib.orc_row_parallel_ring.argtypes = [ctypes.c_int, _i64, _i64, _i64, _f, _i64, _f,
                                           _i64, _f, ctypes.c_int, _d, _i64]
+    lib.orc_quantize_fp8_rows.argtypes = [_i64, _i64, _f, _i64, _f, _f]
+    lib.orc_column_parallel_fp8.argtypes = [ctypes.c_int, _i64, _i64, _i64, _f, _i64, _f, _f,
+                                            _i64, _f, _f, _f, ctypes.c_int, _d, _i64]
+    lib.orc_row_parallel_fp8.argtypes = [ctypes.c_int, _i64, _i64, _i64, _f, _i64, _f, _i64, _f,
+                                         _f, _d, _i64]
     lib.orc_mlp_block.argtypes = [ctypes.c_int, _i64, _i64, _i64, ctypes.c_int, _f,
                                   _f, _f, _f, _f, _f, ctypes.c_int, _d, _d]
     lib.orc_qkv_proj.argtypes = [ctypes.c_int, _i64, _i64, ctypes.c_int,
@@ -87,6 +92,7 @@ def _bind(lib):
                                _f, _f, _f, _d]
     for name in ("orc_linear", "orc_swiglu", "orc_column_parallel",
                  "orc_column_parallel_uneven", "orc_row_parallel", "orc_row_parallel_ring",
+                 "orc_quantize_fp8_rows", "orc_column_parallel_fp8", "orc_row_parallel_fp8",
                  "orc_mlp_block",
                  "orc_qkv_proj", "orc_o_proj"):
         getattr(lib, name).restype = ctypes.c_int
@@ -210,6 +216,53 @@ class Oracle:
                                                1 if wire == "bf16" else 0, _pd(Y), N),
                "row_parallel_ring")
         return Y
+
+    # ------------------------------------------------------------ FP8 weights
+    def round_e4m3(self, x: float) -> float:
+        return self._lib.orc_round_e4m3(float(x))
+
+    def quantize_rows_fp8(self, W):
+        """Per-row e4m3 quantization: (Q as float32 e4m3 values, S fp32 row scales)."""
+        W = _f32(W)
+        R, C = W.shape
+        Q = np.empty((R, C), dtype=np.float32)
+        S = np.empty((R,), dtype=np.float32)
+        _check(self._lib.orc_quantize_fp8_rows(R, C, _pf(W), C, _pf(Q), _pf(S)), "quantize_fp8")
+        return Q, S
+
+    def column_parallel_fp8(self, tp, X, Q, S, b=None, act="none", Qu=None, Su=None):
+        """Column split with FP8 weights: act(S[n] * (x . Q[n]) + b[n]) (SwiGLU: gate/up)."""
+        X, Q, Qu, S, Su, b = (_f32(a) for a in (X, Q, Qu, S, Su, b))
+        M, K = X.shape
+        N = Q.shape[0]
+        Y = np.empty((M, N), dtype=np.float64)
+        _check(self._lib.orc_column_parallel_fp8(tp, M, K, N, _pf(X), K, _pf(Q), _pf(Qu), K,
+                                                 _pf(S), _pf(Su), _pf(b), _act(act), _pd(Y), N),
+               "column_parallel_fp8")
+        return Y
+
+    def row_parallel_fp8(self, tp, X, Q, S, b=None):
+        """Row split with FP8 weights: sum_i S_i[n] * (x_i . Q_i[n]) + b; S is [tp, N]."""
+        X, Q, S, b = (_f32(a) for a in (X, Q, S, b))
+        M, K = X.shape
+        N = Q.shape[0]
+        Y = np.empty((M, N), dtype=np.float64)
+        _check(self._lib.orc_row_parallel_fp8(tp, M, K, N, _pf(X), K, _pf(Q), K, _pf(S),
+                                              _pf(b), _pd(Y), N), "row_parallel_fp8")
+        return Y
+
+    def quantize_row_shards_fp8(self, tp, W):
+        """Quantize each row-split shard [N, K/tp] of W on its own: (Q [N, K], S [tp, N])."""
+        W = _f32(W)
+        N, K = W.shape
+        ks = K // tp
+        Q = np.empty((N, K), dtype=np.float32)
+        S = np.empty((tp, N), dtype=np.float32)
+        for i in range(tp):
+            q, s = self.quantize_rows_fp8(W[:, i * ks:(i + 1) * ks])
+            Q[:, i * ks:(i + 1) * ks] = q
+            S[i] = s
+        return Q, S
 
     def round_f32(self, x: float) -> float:
         return self._lib.orc_round_f32(float(x))

@@ -327,6 +327,122 @@ int orc_row_parallel_ring(int tp, int64_t M, int64_t K, int64_t N, const float* 
   return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* FP8 (e4m3) weights with one fp32 scale per weight row                     */
+/* ------------------------------------------------------------------------ */
+/*
+ * "Model Parallelism" (statistical-learning-notes) sizes weights at about one
+ * byte per parameter in FP8; no page fixes the format or the scaling.
+ * Readings: e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, largest finite value 448); one fp32 scale per weight row,
+ * s = max_k |W[r,k]| / 448 (1 for an all-zero row); the code is W[r,k] / s
+ * rounded to e4m3, ties to even, saturating at +-448.  The scale and the
+ * division are done in fp32: that is the precision in which the code is
+ * decided.  The dequantized weight is s * q.
+ */
+
+/* Round to the nearest e4m3 value, ties to even, saturating at +-448. */
+double orc_round_e4m3(double x) {
+  if (isnan(x) || x == 0.0) return x;
+  double a = fabs(x);
+  double r;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: quantum 2^-9 */
+    r = ldexp(nearbyint(ldexp(a, 9)), -9);
+  } else {
+    int e;
+    double m = frexp(a, &e);                     /* a = m * 2^e, m in [0.5, 1) */
+    r = ldexp(nearbyint(ldexp(m, 4)), e - 4);    /* keep 4 significant bits */
+  }
+  if (r > 448.0) r = 448.0;
+  return x < 0 ? -r : r;
+}
+
+/*
+ * Per-row quantization of W [rows, cols] (row stride ldw): S[r] = the row's
+ * scale, Q[r*cols + c] = the e4m3 value of W[r,c] / S[r] (as a float).
+ */
+int orc_quantize_fp8_rows(int64_t rows, int64_t cols, const float* W, int64_t ldw, float* Q,
+                          float* S) {
+  if (rows < 0 || cols < 0) return ORC_ERR_BAD_SHAPE;
+  if (rows * cols > 0 && (!W || !Q || !S)) return ORC_ERR_NULL;
+  for (int64_t r = 0; r < rows; ++r) {
+    float amax = 0.0f;
+    for (int64_t c = 0; c < cols; ++c) {
+      const float v = fabsf(W[r * ldw + c]);
+      if (v > amax) amax = v;
+    }
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    S[r] = sc;
+    for (int64_t c = 0; c < cols; ++c) {
+      const float v = W[r * ldw + c] / sc; /* fp32 division */
+      Q[r * cols + c] = (float)orc_round_e4m3((double)v);
+    }
+  }
+  return ORC_OK;
+}
+
+/*
+ * Column-parallel linear with FP8 weights [the column split of
+ * orc_column_parallel]: output n of shard i is act(S[n] * (x . Q[n]) + b[n]),
+ * SwiGLU: silu(S[n] * (x . Q[n])) * (Su[n] * (x . Qu[n])).  Q/Qu hold the e4m3
+ * values (as floats) of the unsharded [N, K] weights, S/Su their row scales;
+ * shard i is rows [i*N/p, (i+1)*N/p) of each.
+ */
+int orc_column_parallel_fp8(int tp, int64_t M, int64_t K, int64_t N, const float* X,
+                            int64_t ldx, const float* Q, const float* Qu, int64_t ldq,
+                            const float* S, const float* Su, const float* b, int act, double* Y,
+                            int64_t ldy) {
+  if (tp < 1) return ORC_ERR_BAD_SHAPE;
+  if (N % tp != 0) return ORC_ERR_NOT_DIVISIBLE;
+  if (act == ORC_ACT_SWIGLU && (!Qu || !Su)) return ORC_ERR_NULL;
+  const int64_t ns = N / tp;
+  for (int i = 0; i < tp; ++i) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+      for (int64_t j = 0; j < ns; ++j) {
+        const int64_t n = (int64_t)i * ns + j; /* row of shard i, column block i of Y */
+        double z = (double)S[n] * dot(K, X + m * ldx, Q + n * ldq);
+        if (act == ORC_ACT_SWIGLU) {
+          const double u = (double)Su[n] * dot(K, X + m * ldx, Qu + n * ldq);
+          z = orc_silu(z) * u;
+        } else {
+          if (b) z += (double)b[n];
+          z = apply_act(act, z);
+        }
+        Y[m * ldy + n] = z;
+      }
+  }
+  return ORC_OK;
+}
+
+/*
+ * Row-parallel linear with FP8 weights [the row split of orc_row_parallel]:
+ * shard i holds columns [i*K/p, (i+1)*K/p) of Q (e4m3 values of the
+ * unsharded [N, K] weight, row stride ldq), quantized as its own [N, K/p]
+ * matrix with row scales S[i*N + n].  Its partial is S_i[n] * (x_i . Q_i[n]);
+ * the partials are summed in shard order, then the bias is added once.
+ */
+int orc_row_parallel_fp8(int tp, int64_t M, int64_t K, int64_t N, const float* X, int64_t ldx,
+                         const float* Q, int64_t ldq, const float* S, const float* b, double* Y,
+                         int64_t ldy) {
+  if (tp < 1) return ORC_ERR_BAD_SHAPE;
+  if (M < 0 || K < 0 || N < 0) return ORC_ERR_BAD_SHAPE;
+  if (K % tp != 0) return ORC_ERR_NOT_DIVISIBLE;
+  const int64_t ks = K / tp;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double y = 0.0;
+      for (int i = 0; i < tp; ++i)
+        y += (double)S[(int64_t)i * N + n] *
+             dot(ks, X + m * ldx + (int64_t)i * ks, Q + n * ldq + (int64_t)i * ks);
+      if (b) y += (double)b[n];
+      Y[m * ldy + n] = y;
+    }
+  return ORC_OK;
+}
+
 /*
  * FFN block: column-parallel first linear with the nonlinearity applied per
  * shard, then row-parallel second linear whose shard-i input is h_i

@@ -304,6 +304,60 @@ def check_ring_allreduce(orc):
         raise AssertionError("row_parallel_ring accepted tp=3 with K=4")
 
 
+def check_fp8_weights(orc):
+    """FP8 (e4m3) weights with per-row scales: rounding against torch's
+    float8_e4m3fn conversion and hand-worked ties, the quantizer against its
+    invariants, the FP8 column and row splits against numpy fp64 matmuls."""
+    # e4m3: 4 significant bits, spacing 1/8 in [1,2) and 2 in [16,32),
+    # subnormal quantum 2^-9, saturation at 448; ties to even
+    for x, want in [(448.0, 448.0), (449.0, 448.0), (1e6, 448.0), (1.0625, 1.0), (1.1875, 1.25),
+                    (17.0, 16.0), (19.0, 20.0), (2.0 ** -10, 0.0), (3 * 2.0 ** -10, 2.0 ** -8),
+                    (-0.3, -0.3125), (0.0625, 0.0625)]:
+        assert orc.round_e4m3(x) == want, (x, orc.round_e4m3(x), want)
+    v = (torch.from_numpy(_rng(5).standard_normal(20000).astype(np.float32)) * 60).clamp(-448, 448)
+    ref = v.to(torch.float8_e4m3fn).double().numpy()
+    mine = np.array([orc.round_e4m3(float(x)) for x in v.double().numpy()])
+    assert np.array_equal(mine, ref)
+    # quantizer invariants
+    rng = _rng(8)
+    W = (rng.standard_normal((6, 40)) * rng.uniform(0.01, 3, (6, 1))).astype(np.float32)
+    W[3] = 0.0
+    Q, S = orc.quantize_rows_fp8(W)
+    assert S[3] == 1.0 and not np.any(Q[3])
+    for r in (0, 1, 2, 4, 5):
+        assert np.max(np.abs(Q[r])) == 448.0             # the row maximum maps to 448
+        err = np.abs(S[r].astype(np.float64) * Q[r] - W[r])
+        assert np.all(err <= S[r] * (np.abs(Q[r]) * 2.0 ** -4 + 2.0 ** -10) * 1.0001)
+    assert all(orc.round_e4m3(float(q)) == q for q in Q.ravel()[:200])
+    Q2, S2 = orc.quantize_rows_fp8(2 * W)                # a power of 2 scales exactly
+    assert np.array_equal(Q2, Q) and np.array_equal(S2[[0, 1, 2, 4, 5]], 2 * S[[0, 1, 2, 4, 5]])
+    # FP8 column split (none / GELU / SwiGLU) against numpy on the dequantized weight
+    X = rng.standard_normal((3, 40)).astype(np.float32)
+    b = rng.standard_normal(6).astype(np.float32)
+    Wd = S.astype(np.float64)[:, None] * Q
+    lin = X.astype(np.float64) @ Wd.T
+    for tp in (1, 2, 3):
+        assert _rel_err(orc.column_parallel_fp8(tp, X, Q, S, b), lin + b) < 1e-13
+        g = orc.column_parallel_fp8(tp, X, Q, S, b, "gelu")
+        z = lin + b
+        assert _rel_err(g, z * scipy.special.ndtr(z)) < 1e-12
+    Qu, Su = orc.quantize_rows_fp8(W[::-1].copy())
+    up = X.astype(np.float64) @ (Su.astype(np.float64)[:, None] * Qu).T
+    sw = orc.column_parallel_fp8(2, X, Q, S, act="swiglu", Qu=Qu, Su=Su)
+    assert _rel_err(sw, lin * scipy.special.expit(lin) * up) < 1e-12
+    # FP8 row split: every shard quantized on its own, scaled, summed, + b once
+    W = rng.standard_normal((5, 48)).astype(np.float32)
+    X = rng.standard_normal((2, 48)).astype(np.float32)
+    b = rng.standard_normal(5).astype(np.float32)
+    for tp in (1, 2, 3, 4):
+        Q, S = orc.quantize_row_shards_fp8(tp, W)
+        ks = 48 // tp
+        want = sum(X[:, i * ks:(i + 1) * ks].astype(np.float64) @
+                   (S[i].astype(np.float64)[:, None] * Q[:, i * ks:(i + 1) * ks]).T
+                   for i in range(tp)) + b
+        assert _rel_err(orc.row_parallel_fp8(tp, X, Q, S, b), want) < 1e-13
+
+
 def check_divisibility_errors(orc):
     """tp must divide out_features (column), in_features (row) and the heads."""
     import oracle
@@ -399,6 +453,7 @@ ALL_CHECKS = [
     check_uneven_split,
     check_divisibility_errors,
     check_ring_allreduce,
+    check_fp8_weights,
     check_mlp_block,
     check_attention_projections,
 ]

@@ -37,6 +37,13 @@ MUTANTS = [
     ("ring_direction", "const int r = (c + s) % tp;", "const int r = (c + tp - s) % tp;"),
     ("ring_no_hop_rounding", "acc = wire_bf16 ? orc_round_bf16(acc) : orc_round_f32(acc);", ";"),
     ("ring_chunk_start_rank0", "double acc = part[(int64_t)c * L + e];", "double acc = part[e];"),
+    ("e4m3_3_bits", "r = ldexp(nearbyint(ldexp(m, 4)), e - 4);", "r = ldexp(nearbyint(ldexp(m, 3)), e - 3);"),
+    ("e4m3_no_saturation", "if (r > 448.0) r = 448.0;", ";"),
+    ("fp8_scale_e5m2_max", "const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;",
+     "const float sc = amax > 0.0f ? amax / 57344.0f : 1.0f;"),
+    ("fp8_row_scale_shard0", "y += (double)S[(int64_t)i * N + n] *", "y += (double)S[n] *"),
+    ("fp8_column_scale_dropped", "double z = (double)S[n] * dot(K, X + m * ldx, Q + n * ldq);",
+     "double z = dot(K, X + m * ldx, Q + n * ldq);"),
     ("ring_partial_not_rounded",
      "for (int64_t e = 0; e < L; ++e) pi[e] = wire_bf16 ? orc_round_bf16(pi[e]) : orc_round_f32(pi[e]);",
      ";"),
