@@ -63,6 +63,12 @@ WORKLOADS = {
     # (up projection of the decode FFN, 8 tokens, widths 9558/9557/9557)
     "column_uneven_decode_tp3_b8": dict(kind="uneven", M=8, d=8192, dff=28672, tp=3,
                                         widths=(9558, 9557, 9557)),
+    # the decode FFN with e4m3 weights (one byte per weight, one fp32 scale per
+    # weight row): the weights it streams are half the bf16 ones
+    "swiglu_ffn_decode_tp4_b1_fp8": dict(kind="ffn", M=1, d=8192, dff=28672, tp=4,
+                                         act="swiglu", bias=False, fp8=True),
+    "swiglu_ffn_decode_tp4_b8_fp8": dict(kind="ffn", M=8, d=8192, dff=28672, tp=4,
+                                         act="swiglu", bias=False, fp8=True),
 }
 
 # Link bandwidth for the analytic ring all-reduce time of "Tensor parallel
@@ -84,7 +90,8 @@ DEFAULT_WORKLOAD = "swiglu_ffn_prefill_tp8"
 def kernel_work(w):
     """Algorithmic FLOPs and minimum HBM bytes of each kernel launch of one step.
 
-    bf16 operands (2 bytes), fp32 biases, bf16 intermediate h, bf16 output.
+    bf16 operands (2 bytes), fp32 biases, bf16 intermediate h, bf16 output;
+    FP8 workloads: one byte per weight plus one fp32 scale per weight row.
     """
     M, d = w["M"], w["d"]
     if w["kind"] == "row_ring":
@@ -108,6 +115,11 @@ def kernel_work(w):
         col_bytes = 2.0 * (n_w1 * dff * d + M * d + M * dff) + (4 * dff if w.get("bias") else 0)
         row_flops = 2.0 * M * dff * d
         row_bytes = 2.0 * (d * dff + M * dff + M * d) + (4 * d if w.get("bias") else 0)
+        if w.get("fp8"):
+            # weights at one byte instead of two; per-row scales (the row split
+            # holds one scale per output row in each of its tp shards)
+            col_bytes += -1.0 * n_w1 * dff * d + 4.0 * n_w1 * dff
+            row_bytes += -1.0 * d * dff + 4.0 * w["tp"] * d
         return {"column": (col_flops, col_bytes), "row": (row_flops, row_bytes)}
     H, Hkv, hd = w["H"], w["Hkv"], w["hd"]
     nq = (H + 2 * Hkv) * hd
@@ -306,6 +318,11 @@ class Path:
             self.w1, self.b1 = tpla.tp_shard_weights(split, tp, f.W1, W_up=f.W_up, b=f.b1)
             self.w2, _ = tpla.tp_shard_weights("row", tp, f.W2)
             self.b2 = f.b2
+            if w.get("fp8"):
+                # e4m3 codes + row scales replace the bf16 shards
+                self.q1, self.s1 = tpla.quantize_shards_fp8(self.w1)
+                self.q2, self.s2 = tpla.quantize_shards_fp8(self.w2)
+                self.w1 = self.w2 = None
             self.X = f.X
             self.h = torch.empty(w["M"], w["dff"], dtype=torch.bfloat16, device=device)
             self.Y = torch.empty(w["M"], w["d"], dtype=torch.bfloat16, device=device)
@@ -358,6 +375,15 @@ class Path:
     # CUDA event can sit between them.  The attention step is timed whole.
     def parts(self):
         w, t = self.w, self.tpla
+        if w["kind"] == "ffn" and w.get("fp8"):
+            def column(s):
+                t.column_parallel_linear_fp8(w["tp"], self.X, self.q1, self.s1, self.b1, w["act"],
+                                             Y=self.h, N=w["dff"], stream=s)
+
+            def row(s):
+                t.row_parallel_linear_fp8(w["tp"], self.h, self.q2, self.s2, self.b2, Y=self.Y,
+                                          stream=s)
+            return [("column", column), ("row", row)]
         if w["kind"] == "ffn":
             def column(s):
                 t.column_parallel_linear(w["tp"], self.X, self.w1, self.b1, w["act"], Y=self.h,
@@ -391,6 +417,9 @@ class Path:
             self.graph.replay()
             if Y is not self.Y:
                 Y.copy_(self.Y, non_blocking=True)
+        elif w["kind"] == "ffn" and w.get("fp8"):
+            t.tp_mlp_block_fp8(w["tp"], X, self.q1, self.s1, self.b1, self.q2, self.s2, self.b2,
+                               w["act"], d_ff=w["dff"], h=self.h, Y=Y, stream=s)
         elif w["kind"] == "ffn":
             t.tp_mlp_block(w["tp"], X, self.w1, self.b1, self.w2, self.b2, w["act"],
                            d_ff=w["dff"], h=self.h, Y=Y, stream=s)
@@ -571,6 +600,14 @@ def oracle_inputs(w, rows, seed=20_000):
                  b1=None if f.b1 is None else f.b1.cpu().numpy(),
                  b2=None if f.b2 is None else f.b2.cpu().numpy())
         del f
+        if w.get("fp8"):
+            # the oracle's own quantization of the same bf16 weights (input
+            # preparation, outside the timed oracle step)
+            import oracle
+            orc = oracle.default()
+            a["Q1"], a["S1"] = orc.quantize_rows_fp8(a["W1"])
+            a["Q1u"], a["S1u"] = orc.quantize_rows_fp8(a["W1u"])
+            a["Q2"], a["S2"] = orc.quantize_row_shards_fp8(w["tp"], a["W2"])
         return a
     at = inputs.attn(seed, w["M"], w["d"], w["H"], w["Hkv"], w["hd"], device=dev)
     a = dict(X=at.X[rows].float().cpu().numpy(), Wqkv=at.Wqkv.float().cpu().numpy(),
@@ -590,6 +627,13 @@ def oracle_step(orc, w, a):
         return
     if w["kind"] == "uneven":
         orc.column_parallel_uneven(list(w["widths"]), a["X"], a["W1"])
+        return
+    if w["kind"] == "ffn" and w.get("fp8"):
+        import numpy as np
+        h = orc.column_parallel_fp8(w["tp"], a["X"], a["Q1"], a["S1"], None, w["act"],
+                                    Qu=a["Q1u"], Su=a["S1u"])
+        h = np.vectorize(orc.round_bf16)(h)
+        orc.row_parallel_fp8(w["tp"], h, a["Q2"], a["S2"], None)
         return
     if w["kind"] == "ffn":
         orc.mlp_block(w["tp"], a["X"], a["W1"], a["b1"], a["W2"], a["b2"], w["act"], W1u=a["W1u"],
@@ -702,7 +746,8 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(r["elapsed_max"] / K, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 weights x bf16 activations" if w.get("fp8") else "bf16",
             "data": "synthetic",
             "config": dict(workload_config(args.workload, w, world),
                            l2=("L2 flushed between steps (256 MB write)" if r["flush"] else

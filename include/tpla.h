@@ -282,6 +282,68 @@ tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M
                                         tp_stream_t stream);
 
 /*
+ * FP8 (e4m3) weights for decode-shaped calls -- half the weight bytes of bf16.
+ *
+ * "Model Parallelism" (statistical-learning-notes) sizes weights at about one
+ * byte per parameter in FP8.  No page fixes the format or the scaling; this
+ * library's reading:
+ *   - e4m3 codes (4 exponent bits, bias 7, 3 mantissa bits, no infinities,
+ *     largest finite value 448), one byte per weight, row-major like W;
+ *   - one fp32 scale per weight row, s = max_k |W[r,k]| / 448 (1 for a row of
+ *     zeros); code = W[r,k] / s rounded to nearest even, saturating at 448;
+ *     the scale and the quotient are computed in fp32;
+ *   - y = s * (x . q): the dot product runs in fp32 over the e4m3 values and is
+ *     then multiplied by the row's scale; a row-parallel shard is quantized as
+ *     its own [N, K/tp] matrix, so each shard's partial is scaled by its own s
+ *     before the in-kernel shard sum, and the bias is added once.
+ * Quantize the shards tp_shard_weights produces (for SwiGLU, the packed
+ * gate/up shard: every packed row gets its own scale).  The compute calls take
+ * bf16 activations and at most TP_FP8_MAX_TOKENS tokens (a weight-streaming
+ * GEMV; larger M: TP_ERR_UNSUPPORTED); K (per shard for the row split) must be
+ * a multiple of 16.
+ */
+#define TP_FP8_MAX_TOKENS 8
+
+/*
+ * tp_quantize_fp8 -- per-row e4m3 quantization of a bf16 [rows, cols] device
+ * matrix W (contiguous): Q[rows, cols] (uint8 e4m3 codes), scales[rows]
+ * (fp32).  All device memory owned by the caller.
+ * Errors: TP_ERR_BAD_SHAPE, TP_ERR_NULL, TP_ERR_ALIGNMENT, TP_ERR_CUDA.
+ */
+tp_status tp_quantize_fp8(int64_t rows, int64_t cols, const void* W, void* Q,
+                          float* scales, tp_stream_t stream);
+
+/*
+ * column_parallel_linear_fp8 / row_parallel_linear_fp8 / tp_mlp_block_fp8 --
+ * column_parallel_linear, row_parallel_linear and tp_mlp_block with FP8 weight
+ * shards: q_shards[i] holds shard i's e4m3 codes (same shape as the bf16
+ * shard), scale_shards[i] its fp32 row scales.  xdt must be TP_BF16 (X, and
+ * h of the FFN block, are bf16); other arguments as the bf16 calls.
+ * Errors: as the bf16 calls, TP_ERR_UNSUPPORTED for M > TP_FP8_MAX_TOKENS.
+ */
+tp_status column_parallel_linear_fp8(int tp, int64_t M, int64_t K, int64_t N,
+                                     const void* X, int64_t ldx, tp_dtype xdt,
+                                     const void* const* q_shards,
+                                     const float* const* scale_shards,
+                                     const float* const* b_shards, tp_act act,
+                                     void* Y, int64_t ldy, tp_dtype ydt,
+                                     tp_stream_t stream);
+tp_status row_parallel_linear_fp8(int tp, int64_t M, int64_t K, int64_t N,
+                                  const void* X, int64_t ldx, tp_dtype xdt,
+                                  const void* const* q_shards,
+                                  const float* const* scale_shards,
+                                  const float* b, void* Y, int64_t ldy,
+                                  tp_dtype ydt, tp_stream_t stream);
+tp_status tp_mlp_block_fp8(int tp, int64_t M, int64_t d_model, int64_t d_ff,
+                           tp_act act, const void* X,
+                           const void* const* q1_shards,
+                           const float* const* s1_shards,
+                           const float* const* b1_shards,
+                           const void* const* q2_shards,
+                           const float* const* s2_shards, const float* b2,
+                           void* h, void* Y, tp_dtype ydt, tp_stream_t stream);
+
+/*
  * tp_mlp_block -- the tensor-parallel FFN block: column-parallel first linear
  * with the activation applied per shard, then row-parallel second linear whose
  * shard-i input is h_i, summed in the kernel, + b2 once.

@@ -256,13 +256,14 @@ class Oracle:
         W = _f32(W)
         N, K = W.shape
         ks = K // tp
-        Q = np.empty((N, K), dtype=np.float32)
+        Qs = np.empty((tp, N, ks), dtype=np.float32)
         S = np.empty((tp, N), dtype=np.float32)
         for i in range(tp):
-            q, s = self.quantize_rows_fp8(W[:, i * ks:(i + 1) * ks])
-            Q[:, i * ks:(i + 1) * ks] = q
-            S[i] = s
-        return Q, S
+            # shard i: columns [i*ks, (i+1)*ks) of every row, read in place (row stride K)
+            Wi = W[:, i * ks:].ctypes.data_as(_f)
+            _check(self._lib.orc_quantize_fp8_rows(N, ks, Wi, K, _pf(Qs[i]), _pf(S[i])),
+                   "quantize_fp8")
+        return np.ascontiguousarray(Qs.transpose(1, 0, 2).reshape(N, K)), S
 
     def round_f32(self, x: float) -> float:
         return self._lib.orc_round_f32(float(x))

@@ -366,6 +366,8 @@ int orc_quantize_fp8_rows(int64_t rows, int64_t cols, const float* W, int64_t ld
                           float* S) {
   if (rows < 0 || cols < 0) return ORC_ERR_BAD_SHAPE;
   if (rows * cols > 0 && (!W || !Q || !S)) return ORC_ERR_NULL;
+  /* rows are independent: one row per iteration, any thread */
+#pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r) {
     float amax = 0.0f;
     for (int64_t c = 0; c < cols; ++c) {

@@ -75,6 +75,7 @@ tp_status check_bias_array(const float* const* b, int tp) {
 //   bf16, M > kSkinnyMaxTokens                    tcgen05 prefill GEMM
 tp_status run(const LinearProblem& p, cudaStream_t s) {
   if (p.M == 0) return TP_OK;
+  if (p.fp8) return launch_gemv_fp8(p, s);
   if (p.xdt == TP_BF16 && p.M > kGemvMaxTokens) {
     if (p.M <= kSkinnyMaxTokens) return launch_skinny(p, s);
     return launch_gemm_pair(p, s);
@@ -472,6 +473,111 @@ tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M
     off += widths[i];
   }
   return TP_OK;
+}
+
+tp_status tp_quantize_fp8(int64_t rows, int64_t cols, const void* W, void* Q, float* scales,
+                          tp_stream_t stream) {
+  TP_RET_IF(rows < 0 || cols <= 0, TP_ERR_BAD_SHAPE);
+  if (rows == 0) return TP_OK;
+  TP_RET_IF(!W || !Q || !scales, TP_ERR_NULL);
+  TP_RET_IF(!al_to(W, 2) || !al_to(scales, 4), TP_ERR_ALIGNMENT);
+  return launch_quantize_fp8(W, rows, cols, Q, scales, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status column_parallel_linear_fp8(int tp, int64_t M, int64_t K, int64_t N, const void* X,
+                                     int64_t ldx, tp_dtype xdt, const void* const* q_shards,
+                                     const float* const* scale_shards,
+                                     const float* const* b_shards, tp_act act, void* Y,
+                                     int64_t ldy, tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || K <= 0 || N <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(N % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(xdt != TP_BF16 || !valid_io(xdt, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(!valid_act(act), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(act == TP_ACT_SWIGLU && b_shards, TP_ERR_UNSUPPORTED);
+  TP_RET_IF(M > kFp8MaxTokens, TP_ERR_UNSUPPORTED);
+  TP_RET_IF(ldx < K || ldy < N, TP_ERR_BAD_SHAPE);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(q_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(scale_shards, tp)) != TP_OK, st);
+  TP_RET_IF(!scale_shards, TP_ERR_NULL);
+  TP_RET_IF((st = check_bias_array(b_shards, tp)) != TP_OK, st);
+  TP_RET_IF(!al16(X) || (ldx * 2) % 16 || K % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(q_shards, tp)) != TP_OK, st);
+  LinearProblem p = column_problem(tp, M, K, N, X, ldx, xdt, q_shards, b_shards, act, Y, ldy, ydt,
+                                   N / tp);
+  p.fp8 = true;
+  for (int i = 0; i < tp; ++i) p.wscale[i] = scale_shards[i];
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status row_parallel_linear_fp8(int tp, int64_t M, int64_t K, int64_t N, const void* X,
+                                  int64_t ldx, tp_dtype xdt, const void* const* q_shards,
+                                  const float* const* scale_shards, const float* b, void* Y,
+                                  int64_t ldy, tp_dtype ydt, tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || K <= 0 || N <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(K % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(xdt != TP_BF16 || !valid_io(xdt, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(M > kFp8MaxTokens, TP_ERR_UNSUPPORTED);
+  TP_RET_IF(ldx < K || ldy < N, TP_ERR_BAD_SHAPE);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(q_shards, tp)) != TP_OK, st);
+  TP_RET_IF(!scale_shards, TP_ERR_NULL);
+  TP_RET_IF((st = check_bias_array(scale_shards, tp)) != TP_OK, st);
+  TP_RET_IF(!al16(X) || (ldx * 2) % 16 || (K / tp) % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)) || (b && !al_to(b, 4)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(q_shards, tp)) != TP_OK, st);
+  LinearProblem p = row_problem(tp, M, K, N, X, ldx, xdt, q_shards, b, Y, ldy, ydt);
+  p.fp8 = true;
+  for (int i = 0; i < tp; ++i) p.wscale[i] = scale_shards[i];
+  return run(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_mlp_block_fp8(int tp, int64_t M, int64_t d_model, int64_t d_ff, tp_act act,
+                           const void* X, const void* const* q1_shards,
+                           const float* const* s1_shards, const float* const* b1_shards,
+                           const void* const* q2_shards, const float* const* s2_shards,
+                           const float* b2, void* h, void* Y, tp_dtype ydt,
+                           tp_stream_t stream) {
+  TP_RET_IF(!valid_tp(tp), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(M < 0 || d_model <= 0 || d_ff <= 0, TP_ERR_BAD_SHAPE);
+  TP_RET_IF(d_ff % tp, TP_ERR_NOT_DIVISIBLE);
+  TP_RET_IF(!valid_io(TP_BF16, ydt), TP_ERR_DTYPE);
+  TP_RET_IF(!valid_act(act), TP_ERR_BAD_SHAPE);
+  TP_RET_IF(act == TP_ACT_SWIGLU && b1_shards, TP_ERR_UNSUPPORTED);
+  TP_RET_IF(M > kFp8MaxTokens, TP_ERR_UNSUPPORTED);
+  if (M == 0) return TP_OK;
+  tp_status st;
+  TP_RET_IF(!X || !h || !Y, TP_ERR_NULL);
+  TP_RET_IF((st = check_ptr_array(q1_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_ptr_array(q2_shards, tp)) != TP_OK, st);
+  TP_RET_IF(!s1_shards || !s2_shards, TP_ERR_NULL);
+  TP_RET_IF((st = check_bias_array(s1_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(s2_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_bias_array(b1_shards, tp)) != TP_OK, st);
+  TP_RET_IF(!al16(X) || !al16(h) || d_model % 16 || (d_ff / tp) % 16, TP_ERR_ALIGNMENT);
+  TP_RET_IF(!al_to(Y, esz(ydt)) || (b2 && !al_to(b2, 4)), TP_ERR_ALIGNMENT);
+  TP_RET_IF((st = check_aligned_array(q1_shards, tp)) != TP_OK, st);
+  TP_RET_IF((st = check_aligned_array(q2_shards, tp)) != TP_OK, st);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // h = act(X . W1_i^T + b1_i) in bf16, then Y = sum_i h_i . W2_i^T + b2
+  LinearProblem up = column_problem(tp, M, d_model, d_ff, X, d_model, TP_BF16, q1_shards,
+                                    b1_shards, act, h, d_ff, TP_BF16, d_ff / tp);
+  LinearProblem down = row_problem(tp, M, d_ff, d_model, h, d_ff, TP_BF16, q2_shards, b2, Y,
+                                   d_model, ydt);
+  up.fp8 = down.fp8 = true;
+  for (int i = 0; i < tp; ++i) {
+    up.wscale[i] = s1_shards[i];
+    down.wscale[i] = s2_shards[i];
+  }
+  if ((st = run(up, s)) != TP_OK) return st;
+  return run(down, s);
 }
 
 tp_status tp_mlp_block(int tp, int64_t M, int64_t d_model, int64_t d_ff, tp_act act, tp_dtype xdt,

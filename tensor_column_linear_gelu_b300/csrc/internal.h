@@ -49,6 +49,10 @@ struct LinearProblem {
   int64_t wr[TP_MAX_TP] = {};
   int64_t yoff[TP_MAX_TP] = {};
   bool uneven = false;
+  // FP8 weights: W[i] holds e4m3 codes and wscale[i] the fp32 scale of each
+  // of its rows (the weight-streaming FP8 GEMV runs the problem).
+  bool fp8 = false;
+  const float* wscale[TP_MAX_TP] = {};
 };
 
 // Weight-streaming GEMV on CUDA cores (few tokens; also the fp32 path).
@@ -70,6 +74,13 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream);
 // 128-byte swizzle, out-of-range elements read as zero.
 bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t ld_bytes, uint32_t box_rows);
+
+// FP8 (e4m3) weights: per-row quantizer and the weight-streaming FP8 GEMV
+// (bf16 activations, at most kFp8MaxTokens tokens).
+constexpr int64_t kFp8MaxTokens = 8;
+tp_status launch_quantize_fp8(const void* W, int64_t rows, int64_t cols, void* Q, float* S,
+                              cudaStream_t stream);
+tp_status launch_gemv_fp8(const LinearProblem& p, cudaStream_t stream);
 
 // Ring-ordered sum of per-shard partials ([tp][M][N], wire dtype) + bias.
 tp_status launch_ring_reduce(int tp, int64_t M, int64_t N, const void* parts, int wire_dt,

@@ -84,7 +84,6 @@ constexpr int SK_UMMA_K = 16;
 constexpr int SK_ROW_BYTES = SK_BK * 2;     // 128 bytes per staged row
 constexpr int SK_A_BYTES = 128 * SK_ROW_BYTES;  // the A tile one MMA reads (128 rows)
 constexpr int SK_BN = 256;                  // weight rows per MMA (its N, at most)
-constexpr int SK_TILE_ROWS_MAX = 512;       // weight rows of one B tile (two MMAs)
 constexpr int SK_MAX_STAGES = 16;
 constexpr int SK_ACC_BUFS = 2;              // accumulator buffers, when two fit in TMEM
 constexpr int SK_TMEM_COLS = 512;

@@ -34,6 +34,7 @@ TP_SPLIT_COLUMN, TP_SPLIT_ROW, TP_SPLIT_QKV_HEADS, TP_SPLIT_GATE_UP = 0, 1, 2, 3
 TP_MAX_TP = 16
 TP_GATE_UP_GROUP = 128
 TP_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+TP_FP8_MAX_TOKENS = 8
 
 ACTS = {"none": TP_ACT_NONE, "gelu": TP_ACT_GELU_ERF, "swiglu": TP_ACT_SWIGLU}
 SPLITS = {"column": TP_SPLIT_COLUMN, "row": TP_SPLIT_ROW, "qkv_heads": TP_SPLIT_QKV_HEADS,
@@ -43,8 +44,10 @@ _DT = {torch.float32: TP_F32, torch.bfloat16: TP_BF16}
 # Every symbol include/tpla.h declares.
 EXPORTS = ("tp_status_string", "tp_shard_shape", "tp_shard_weights", "column_parallel_linear",
            "row_parallel_linear", "row_parallel_linear_ring", "tp_shard_weights_uneven",
-           "column_parallel_linear_uneven", "tp_mlp_block", "tp_attn_proj", "tp_layer_forward",
-           "tp_device_status", "tp_selftest_bounded_wait", "tp_mlp_block_noalloc")
+           "column_parallel_linear_uneven", "tp_quantize_fp8", "column_parallel_linear_fp8",
+           "row_parallel_linear_fp8", "tp_mlp_block_fp8", "tp_mlp_block", "tp_attn_proj",
+           "tp_layer_forward", "tp_device_status", "tp_selftest_bounded_wait",
+           "tp_mlp_block_noalloc")
 
 # ----------------------------------------------------------------- prototypes
 _vp = ctypes.c_void_p
@@ -67,6 +70,13 @@ lib.row_parallel_linear_ring.argtypes = [_int, _i64, _i64, _i64, _vp, _i64, _int
 lib.tp_shard_weights_uneven.argtypes = [_int, _i64p, _int, _vp, _i64, _i64, _vp, _vpp, _vpp, _vp]
 lib.column_parallel_linear_uneven.argtypes = [_int, _i64p, _i64, _i64, _vp, _i64, _int, _vpp,
                                               _vpp, _int, _vp, _i64, _int, _vp]
+lib.tp_quantize_fp8.argtypes = [_i64, _i64, _vp, _vp, _vp, _vp]
+lib.column_parallel_linear_fp8.argtypes = [_int, _i64, _i64, _i64, _vp, _i64, _int, _vpp, _vpp,
+                                           _vpp, _int, _vp, _i64, _int, _vp]
+lib.row_parallel_linear_fp8.argtypes = [_int, _i64, _i64, _i64, _vp, _i64, _int, _vpp, _vpp, _vp,
+                                        _vp, _i64, _int, _vp]
+lib.tp_mlp_block_fp8.argtypes = [_int, _i64, _i64, _i64, _int, _vp, _vpp, _vpp, _vpp, _vpp, _vpp,
+                                 _vp, _vp, _vp, _int, _vp]
 lib.tp_mlp_block.argtypes = [_int, _i64, _i64, _i64, _int, _int, _vp, _vpp, _vpp, _vpp, _vp, _vp,
                              _vp, _int, _vp]
 lib.tp_attn_proj.argtypes = [_int, _i64, _i64, _int, _int, _int, _int, _vp, _vpp, _vpp, _vp, _int,
@@ -259,6 +269,79 @@ def column_parallel_linear_uneven(widths: Sequence[int], X: torch.Tensor, w_shar
                                              stream_handle(stream)),
            "column_parallel_linear_uneven")
     return Y
+
+
+def tp_quantize_fp8(W: torch.Tensor, stream=None):
+    """Per-row e4m3 quantization of a bf16 [rows, cols] tensor: (codes uint8, scales fp32)."""
+    rows, cols = W.shape
+    Q = torch.empty(rows, cols, dtype=torch.uint8, device=W.device)
+    S = torch.empty(rows, dtype=torch.float32, device=W.device)
+    _check(lib.tp_quantize_fp8(rows, cols, ptr(W.contiguous()), ptr(Q), ptr(S),
+                               stream_handle(stream)), "tp_quantize_fp8")
+    return Q, S
+
+
+def quantize_shards_fp8(w_shards, stream=None):
+    """Quantize every shard of a tp_shard_weights result: (code shards, scale shards)."""
+    qs = [tp_quantize_fp8(w, stream) for w in w_shards]
+    return [q for q, _ in qs], [s for _, s in qs]
+
+
+def column_parallel_linear_fp8(tp: int, X: torch.Tensor, q_shards, s_shards, b_shards=None,
+                               act="none", out_dtype: Optional[torch.dtype] = None,
+                               Y: Optional[torch.Tensor] = None, N: Optional[int] = None,
+                               stream=None) -> torch.Tensor:
+    """column_parallel_linear with FP8 weight shards (codes + row scales)."""
+    M, K = X.shape
+    if N is None:
+        if _act(act) == TP_ACT_SWIGLU:
+            raise ValueError("pass N (d_ff) for SwiGLU: packed shards are padded")
+        N = q_shards[0].shape[0] * tp
+    if Y is None:
+        Y = torch.empty(M, N, dtype=out_dtype or X.dtype, device=X.device)
+    _check(lib.column_parallel_linear_fp8(tp, M, K, N, ptr(X), X.stride(0), dtype_code(X.dtype),
+                                          ptr_array(q_shards), ptr_array(s_shards),
+                                          ptr_array(b_shards), _act(act), ptr(Y), Y.stride(0),
+                                          dtype_code(Y.dtype), stream_handle(stream)),
+           "column_parallel_linear_fp8")
+    return Y
+
+
+def row_parallel_linear_fp8(tp: int, X: torch.Tensor, q_shards, s_shards,
+                            b: Optional[torch.Tensor] = None,
+                            out_dtype: Optional[torch.dtype] = None,
+                            Y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """row_parallel_linear with FP8 weight shards (codes + row scales)."""
+    M, K = X.shape
+    N = q_shards[0].shape[0]
+    if Y is None:
+        Y = torch.empty(M, N, dtype=out_dtype or X.dtype, device=X.device)
+    _check(lib.row_parallel_linear_fp8(tp, M, K, N, ptr(X), X.stride(0), dtype_code(X.dtype),
+                                       ptr_array(q_shards), ptr_array(s_shards), ptr(b), ptr(Y),
+                                       Y.stride(0), dtype_code(Y.dtype), stream_handle(stream)),
+           "row_parallel_linear_fp8")
+    return Y
+
+
+def tp_mlp_block_fp8(tp: int, X: torch.Tensor, q1_shards, s1_shards, b1_shards, q2_shards,
+                     s2_shards, b2: Optional[torch.Tensor], act="swiglu",
+                     d_ff: Optional[int] = None, out_dtype: Optional[torch.dtype] = None,
+                     h: Optional[torch.Tensor] = None, Y: Optional[torch.Tensor] = None,
+                     stream=None):
+    """The FFN block with FP8 weights.  Returns (Y, h)."""
+    M, d_model = X.shape
+    if d_ff is None:
+        d_ff = q2_shards[0].shape[1] * tp
+    if h is None:
+        h = torch.empty(M, d_ff, dtype=torch.bfloat16, device=X.device)
+    if Y is None:
+        Y = torch.empty(M, d_model, dtype=out_dtype or X.dtype, device=X.device)
+    _check(lib.tp_mlp_block_fp8(tp, M, d_model, d_ff, _act(act), ptr(X), ptr_array(q1_shards),
+                                ptr_array(s1_shards), ptr_array(b1_shards), ptr_array(q2_shards),
+                                ptr_array(s2_shards), ptr(b2), ptr(h), ptr(Y),
+                                dtype_code(Y.dtype), stream_handle(stream)),
+           "tp_mlp_block_fp8")
+    return Y, h
 
 
 def tp_mlp_block(tp: int, X: torch.Tensor, w1_shards, b1_shards, w2_shards,

@@ -157,6 +157,24 @@ rec("uneven_col_swiglu", UC(2, W64(5, 4), 4, 64, A, 64, BF, w2, None, 2, A, 9, B
 rec("uneven_col_ldy", UC(2, W64(5, 4), 4, 64, A, 64, BF, w2, None, 0, A, 8, BF, None))
 rec("uneven_col_M0", UC(2, W64(5, 4), 0, 64, None, 64, BF, None, None, 0, None, 9, BF, None))
 rec("uneven_col_width0", UC(2, W64(9, 0), 4, 64, A, 64, BF, w2, None, 0, A, 9, BF, None))
+# FP8 weights
+QZ = L.tp_quantize_fp8
+rec("fp8_quant_rows0", QZ(0, 64, None, None, None, None))
+rec("fp8_quant_null", QZ(4, 64, A, None, A, None))
+rec("fp8_quant_cols0", QZ(4, 0, A, A, A, None))
+CF = L.column_parallel_linear_fp8
+rec("fp8_col_f32_x", CF(2, 4, 64, 64, A, 64, F32, w2, w2, None, 0, A, 64, F32, None))
+rec("fp8_col_too_many_tokens", CF(2, 9, 64, 64, A, 64, BF, w2, w2, None, 0, A, 64, BF, None))
+rec("fp8_col_null_scales", CF(2, 4, 64, 64, A, 64, BF, w2, None, None, 0, A, 64, BF, None))
+rec("fp8_col_K_not16", CF(2, 4, 72, 64, A, 72, BF, w2, w2, None, 0, A, 64, BF, None))
+rec("fp8_col_swiglu_bias", CF(2, 4, 64, 64, A, 64, BF, w2, w2, w2, 2, A, 64, BF, None))
+RF = L.row_parallel_linear_fp8
+rec("fp8_row_shardK_not16", RF(2, 4, 48, 64, A, 48, BF, w2, w2, None, A, 64, BF, None))
+rec("fp8_row_notdiv", RF(3, 4, 64, 64, A, 64, BF, arr(A, A, A), arr(A, A, A), None, A, 64, BF, None))
+rec("fp8_row_M0", RF(2, 0, 64, 64, None, 64, BF, None, None, None, None, 64, BF, None))
+MF = L.tp_mlp_block_fp8
+rec("fp8_mlp_null_h", MF(2, 4, 64, 128, 2, A, w2, w2, None, w2, w2, None, None, A, BF, None))
+rec("fp8_mlp_too_many", MF(2, 16, 64, 128, 2, A, w2, w2, None, w2, w2, None, A, A, BF, None))
 json.dump(res, sys.stdout)
 '''
 
@@ -178,6 +196,10 @@ EXPECT = {
     "ring_notdiv": 2, "ring_M0": 0, "ring_bad_wire": 4, "uneven_shard_sum": 3,
     "uneven_shard_zero": 3, "uneven_shard_null_widths": 1, "uneven_col_swiglu": 8,
     "uneven_col_ldy": 3, "uneven_col_M0": 0, "uneven_col_width0": 3,
+    "fp8_quant_rows0": 0, "fp8_quant_null": 1, "fp8_quant_cols0": 3, "fp8_col_f32_x": 4,
+    "fp8_col_too_many_tokens": 8, "fp8_col_null_scales": 1, "fp8_col_K_not16": 5,
+    "fp8_col_swiglu_bias": 8, "fp8_row_shardK_not16": 5, "fp8_row_notdiv": 2, "fp8_row_M0": 0,
+    "fp8_mlp_null_h": 1, "fp8_mlp_too_many": 8,
 }
 
 
