@@ -298,11 +298,13 @@ tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M
  *     before the in-kernel shard sum, and the bias is added once.
  * Quantize the shards tp_shard_weights produces (for SwiGLU, the packed
  * gate/up shard: every packed row gets its own scale).  The compute calls take
- * bf16 activations and at most TP_FP8_MAX_TOKENS tokens (a weight-streaming
- * GEMV; larger M: TP_ERR_UNSUPPORTED); K (per shard for the row split) must be
- * a multiple of 16.
+ * bf16 activations and at most TP_FP8_MAX_TOKENS tokens (decode shapes: a
+ * weight-streaming GEMV for one or two tokens, the tensor-core decode kernel,
+ * which widens the codes to bf16 on chip, for more; larger M:
+ * TP_ERR_UNSUPPORTED); K (per shard for the row split) must be a multiple of
+ * 16.  The column split stays bit-identical to tp = 1.
  */
-#define TP_FP8_MAX_TOKENS 8
+#define TP_FP8_MAX_TOKENS 128
 
 /*
  * tp_quantize_fp8 -- per-row e4m3 quantization of a bf16 [rows, cols] device

@@ -73,9 +73,16 @@ tp_status check_bias_array(const float* const* b, int tp) {
 //   fp32, or bf16 with M <= kGemvMaxTokens      weight-streaming GEMV (CUDA cores)
 //   bf16, kGemvMaxTokens < M <= kSkinnyMaxTokens  tcgen05 decode kernel
 //   bf16, M > kSkinnyMaxTokens                    tcgen05 prefill GEMM
+//   FP8 weights, M <= kGemvMaxTokens              FP8 weight-streaming GEMV
+//   FP8 weights, larger M                         tcgen05 decode kernel, FP8 mode
+// (FP8 row-parallel calls with tp above the decode kernel's largest cluster
+// also take the FP8 GEMV: its CTAs must each hold one shard's k-range.)
 tp_status run(const LinearProblem& p, cudaStream_t s) {
   if (p.M == 0) return TP_OK;
-  if (p.fp8) return launch_gemv_fp8(p, s);
+  if (p.fp8) {
+    if (p.M > kGemvMaxTokens && !(p.row && p.tp > kSkinnyMaxCluster)) return launch_skinny(p, s);
+    return launch_gemv_fp8(p, s);
+  }
   if (p.xdt == TP_BF16 && p.M > kGemvMaxTokens) {
     if (p.M <= kSkinnyMaxTokens) return launch_skinny(p, s);
     return launch_gemm_pair(p, s);

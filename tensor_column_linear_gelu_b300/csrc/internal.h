@@ -50,7 +50,7 @@ struct LinearProblem {
   int64_t yoff[TP_MAX_TP] = {};
   bool uneven = false;
   // FP8 weights: W[i] holds e4m3 codes and wscale[i] the fp32 scale of each
-  // of its rows (the weight-streaming FP8 GEMV runs the problem).
+  // of its rows.
   bool fp8 = false;
   const float* wscale[TP_MAX_TP] = {};
 };
@@ -62,9 +62,11 @@ tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream);
 // tokens; 256 x 256 tiles).
 tp_status launch_gemm_pair(const LinearProblem& p, cudaStream_t stream);
 
-// tcgen05 decode kernel with the weights as the MMA's M operand (bf16; a
-// handful of tokens, up to kSkinnyMaxTokens).
+// tcgen05 decode kernel with the weights as the MMA's N operand (a handful
+// of tokens, up to kSkinnyMaxTokens; bf16 weights, or e4m3 weights widened
+// to bf16 in shared memory when p.fp8).
 constexpr int64_t kSkinnyMaxTokens = 128;
+constexpr int kSkinnyMaxCluster = 8;  // CTAs per cluster on its row side
 // bf16 calls with at most this many tokens go to the GEMV.
 constexpr int64_t kGemvMaxTokens = 2;
 tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream);
@@ -75,9 +77,17 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream);
 bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t ld_bytes, uint32_t box_rows);
 
-// FP8 (e4m3) weights: per-row quantizer and the weight-streaming FP8 GEMV
-// (bf16 activations, at most kFp8MaxTokens tokens).
-constexpr int64_t kFp8MaxTokens = 8;
+// 2-D byte tensor map (e4m3 codes): boxes of box_inner bytes (a multiple of
+// 16, at most 256) x box_rows rows, no swizzle (rows land box_inner bytes
+// apart), out-of-range bytes read as zero.
+bool make_tma_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                     uint64_t ld_bytes, uint32_t box_inner, uint32_t box_rows);
+
+// FP8 (e4m3) weights, bf16 activations, at most kFp8MaxTokens tokens: the
+// per-row quantizer; the weight-streaming FP8 GEMV (M <= kGemvMaxTokens, and
+// row-parallel calls whose tp exceeds the largest cluster); otherwise the
+// decode kernel in its FP8 mode (launch_skinny with p.fp8).
+constexpr int64_t kFp8MaxTokens = kSkinnyMaxTokens;
 tp_status launch_quantize_fp8(const void* W, int64_t rows, int64_t cols, void* Q, float* S,
                               cudaStream_t stream);
 tp_status launch_gemv_fp8(const LinearProblem& p, cudaStream_t stream);

@@ -46,7 +46,7 @@
 // Parallelism Works Under the Hood"; "Tensor parallel serving",
 // "Column-parallel and row-parallel layers, paired".)
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (192 threads, 704 in FP8 mode; one CTA per SM):
 //   warp 0      TMA producer: per k-block one X box {64, xrows} (lane 0) and
 //               the tile's weight rows as 64-row and 16-row boxes, one box
 //               per lane: a single thread issuing many small boxes cannot
@@ -60,6 +60,31 @@
 //               bias / activation in fp32, one rounding, row stores; on the
 //               row side the partial goes to shared memory for the cluster
 //               reduction.
+//   warps 6-21  FP8 mode only: the converters (below).
+//
+// FP8 mode (e4m3 weight codes + one fp32 scale per weight row).  The codes
+// are streamed at one byte per weight -- half the bytes of bf16, which is the
+// point for a call bound by weight bytes -- and widened on chip:
+//   * the producer loads the same boxes as in bf16 mode, 64 codes wide, into
+//     a ring of raw stages (rows 64 bytes apart, no swizzle);
+//   * sixteen converter warps (two groups taking alternate k-blocks) turn
+//     each k-block of a raw stage into a bf16 B tile laid out
+//     exactly as a 128-byte-swizzled TMA load would have left it (16-byte
+//     chunk c of row r at chunk c ^ (r mod 8)), fence the writes for the
+//     async proxy and hand the buffer to the MMA thread.  The widening is
+//     exact (every e4m3 value is a bf16 value), so the MMA computes x . q in
+//     fp32 as the bf16 path computes x . w;
+//   * the epilogue multiplies each output's accumulator by its weight row's
+//     scale (gate and up rows each by their own) before the bias and the
+//     activation.  On the row side each CTA's k-range lies inside one shard
+//     (clusters of tp x j CTAs), so its partial is scaled by that shard's row
+//     scales before the cluster sum.
+// Three rings: X boxes (released by the MMA's commit), raw code stages
+// (released by the converters as soon as they are read, so that most of the
+// raw ring is always in flight from HBM) and two bf16 B-tile buffers between
+// the converters and the MMA thread.  A B tile holds at most 256 rows (one
+// MMA), which keeps the bf16 buffers small and the raw ring deep.
+//
 // Every mbarrier wait is bounded (sync.cuh); a wait that gives up records the
 // failure in the device error word and that role stops issuing work.  Every
 // thread of every CTA still reaches both cluster barriers, so a failure can
@@ -79,9 +104,31 @@ namespace {
 
 constexpr int SK_THREADS = 192;
 constexpr int SK_EPI_WARP0 = 2;
+constexpr int SK_CONV_WARP0 = 6;            // FP8 mode: first converter warp
+constexpr int SK_CONV_WARPS = 16;
+// Two converter groups take alternate k-blocks, each into its own bf16
+// buffer, so that two conversions are in progress at any time.
+constexpr int SK_CONV_GROUPS = 2;
+constexpr int SK_GROUP_WARPS = SK_CONV_WARPS / SK_CONV_GROUPS;
+constexpr int SK_GROUP_THREADS = 32 * SK_GROUP_WARPS;
+// a converter thread's rows advance by SK_GROUP_THREADS / 4 per chunk, a
+// multiple of 8: its swizzle phase (row mod 8) never changes
+static_assert((SK_GROUP_THREADS / 4) % 8 == 0, "converter row stride");
+constexpr int SK_THREADS_F8 = SK_THREADS + 32 * SK_CONV_WARPS;
 constexpr int SK_BK = 64;                   // k per stage: one 128-byte swizzle span
 constexpr int SK_UMMA_K = 16;
-constexpr int SK_ROW_BYTES = SK_BK * 2;     // 128 bytes per staged row
+constexpr int SK_ROW_BYTES = SK_BK * 2;     // 128 bytes per staged bf16 row
+// FP8 mode: a raw stage holds SK_F8_KPR k-blocks of each tile row, so that
+// every TMA row request moves SK_F8_KPR x 64 contiguous bytes of codes
+#ifndef SK_F8_KPR
+#define SK_F8_KPR 2
+#endif
+constexpr int SK_KPR = SK_F8_KPR;
+static_assert(SK_KPR == 1 || SK_KPR == 2 || SK_KPR == 4, "k-blocks per raw stage");
+constexpr int SK_RAW_ROW_BYTES = SK_BK * SK_KPR;  // bytes per staged row of codes
+constexpr int SK_CSTAGES = 2;               // FP8 mode: bf16 B-tile buffers, one per group
+constexpr int SK_MAX_CSTAGES = 4;
+static_assert(SK_CSTAGES == SK_CONV_GROUPS, "k-block n uses buffer n mod 2, converted by group n mod 2");
 constexpr int SK_A_BYTES = 128 * SK_ROW_BYTES;  // the A tile one MMA reads (128 rows)
 constexpr int SK_BN = 256;                  // weight rows per MMA (its N, at most)
 constexpr int SK_MAX_STAGES = 16;
@@ -89,9 +136,9 @@ constexpr int SK_ACC_BUFS = 2;              // accumulator buffers, when two fit
 constexpr int SK_TMEM_COLS = 512;
 constexpr int SK_GRAIN = 16;                // features per balance unit (column side)
 constexpr int SK_MAX_BOXES = 31;            // weight boxes per stage (one per producer lane)
-constexpr int SK_MAX_CLUSTER = 8;
+constexpr int SK_MAX_CLUSTER = kSkinnyMaxCluster;
 constexpr int SK_RED_PITCH = SK_BN + 4;     // floats per token row of a reduction buffer
-constexpr int SK_NUM_BARS = 2 * SK_MAX_STAGES + 2 * SK_ACC_BUFS + 1;
+constexpr int SK_NUM_BARS = 4 * SK_MAX_STAGES + 2 * SK_ACC_BUFS + 1 + 2 * SK_MAX_CSTAGES;
 constexpr int SK_BAR_BYTES = SK_NUM_BARS * 8 + 16;
 constexpr int SK_SMEM_MAX = 232448;         // dynamic shared memory per CTA (227 KB)
 constexpr int64_t G = TP_GATE_UP_GROUP;
@@ -99,9 +146,10 @@ static_assert(2 * G == SK_BN, "a gate/up group's rows fill one MMA");
 
 struct SkinnyParams {
   CUtensorMap tmX[TP_MAX_TP];    // column: [0] = X; row: X_i.  Box {64, xrows}.
-  CUtensorMap tmW16[TP_MAX_TP];  // W_i, box {64, 16}
+  CUtensorMap tmW16[TP_MAX_TP];  // W_i, box {64, 16} (FP8 mode: 64 codes x 16 rows)
   CUtensorMap tmW64[TP_MAX_TP];  // W_i, box {64, 64}
   const float* bias[TP_MAX_TP];
+  const float* wscale[TP_MAX_TP];  // FP8 mode: scale of each row of W_i
   void* Y;
   unsigned int* err;
   int64_t ldy;
@@ -111,6 +159,9 @@ struct SkinnyParams {
   int tp, row, act, ydt;
   int xrows, x_stage_bytes, stages;
   int w_stage_bytes;             // weight rows of a B tile x 128 bytes
+  int raw_stage_bytes;           // FP8 mode: weight rows of a B tile x 64 bytes
+  int cstages;                   // FP8 mode: bf16 B-tile buffers
+  int xstages;                   // FP8 mode: X ring depth (the raw ring has `stages`)
   int tile_cap;                  // column: features (SwiGLU) or rows per tile
   int acc_stride, acc_bufs;      // TMEM columns per accumulator buffer, buffers
   int kb_per_shard, kb_total;
@@ -118,6 +169,37 @@ struct SkinnyParams {
 };
 
 __device__ __forceinline__ int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Byte permute (PTX prmt, default mode): result byte i is byte (sel_i & 7)
+// of {a, 0}, or that byte's sign bit replicated when sel_i & 8.
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
+  return r;
+}
+
+// Two e4m3 codes to two bf16 values, exactly.  Each 16-bit lane of w holds a
+// code in its low byte and the code's sign replicated through its high byte:
+// s s s s s s s s | s e e e e m m m.  Shifted left by 4 (the low lane's top
+// nibble spills into bits 0-3 of the high lane, which the mask clears) and
+// masked, a lane keeps the sign at bit 15 and the code's exponent and
+// mantissa at bits 7..10 and 4..6: read as bf16 that is the e4m3 value times
+// 2^-120 (bf16 exponent bias 127 against e4m3's 7; a subnormal code gives the
+// matching subnormal bf16).  One bf16x2 multiply by 2^120 (0x7B80) restores
+// the value; no step rounds.
+__device__ __forceinline__ uint32_t e4m3_lanes_to_bf16x2(uint32_t w) {
+  const uint32_t bits = (w << 4) & 0x87F087F0u;
+  uint32_t out;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(bits), "r"(0x7B807B80u));
+  return out;
+}
+
+// Four e4m3 codes (code k in byte k of q) to four bf16 values: codes 0, 1 in
+// lo (low half first), codes 2, 3 in hi.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t q, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3_lanes_to_bf16x2(prmt_b32(q, 0x9180u));  // bytes: q0, sign(q0), q1, sign(q1)
+  hi = e4m3_lanes_to_bf16x2(prmt_b32(q, 0xB3A2u));  // bytes: q2, sign(q2), q3, sign(q3)
+}
 
 constexpr int SK_MAX_PIECES = 8;
 
@@ -238,20 +320,31 @@ __device__ __forceinline__ Tile row_tile(const SkinnyParams& p, int rank) {
     }                                                                 \
   } while (0)
 
-__global__ void __launch_bounds__(SK_THREADS, 1)
+template <bool F8>
+__global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
     skinny_kernel(const __grid_constant__ SkinnyParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // bf16 mode: S X stages, S weight stages (one ring).  FP8 mode: XS X
+  // stages, S raw (e4m3) stages, cstages bf16 B-tile buffers (three rings).
+  // All 1024-byte aligned.
   const int S = p.stages;
-  uint8_t* sX = smem;                                      // S x-stages, then
-  uint8_t* sW = smem + (size_t)S * p.x_stage_bytes;        // S weight stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sW + (size_t)S * p.w_stage_bytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + SK_MAX_STAGES;
-  uint64_t* tfull = bars + 2 * SK_MAX_STAGES;
+  const int XS = F8 ? p.xstages : S;
+  const int WB = F8 ? p.cstages : S;                       // bf16 B-tile buffers
+  uint8_t* sX = smem;
+  uint8_t* sR = smem + (size_t)XS * p.x_stage_bytes;       // FP8 mode only
+  uint8_t* sW = sR + (F8 ? (size_t)S * p.raw_stage_bytes : 0);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sW + (size_t)WB * p.w_stage_bytes);
+  uint64_t* full = bars;                       // X (bf16: X + weights) landed
+  uint64_t* empty = bars + SK_MAX_STAGES;      // X stage consumed by the MMAs
+  uint64_t* rfull = bars + 2 * SK_MAX_STAGES;  // FP8: codes landed
+  uint64_t* rempty = bars + 3 * SK_MAX_STAGES; // FP8: codes read by the converters
+  uint64_t* tfull = bars + 4 * SK_MAX_STAGES;
   uint64_t* tempty = tfull + SK_ACC_BUFS;
   uint64_t* drain = tempty + SK_ACC_BUFS;
+  uint64_t* cfull = drain + 1;                 // FP8: bf16 buffer converted
+  uint64_t* cempty = cfull + SK_MAX_CSTAGES;   // FP8: bf16 buffer consumed by the MMAs
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + SK_NUM_BARS);
   // Row side: after the K loop the ring is reused as this CTA's reduction
   // buffer red[token][SK_RED_PITCH] (fp32).
@@ -261,17 +354,31 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const bool swiglu = (!p.row && p.act == TP_ACT_SWIGLU);
   const int rank = p.row ? (int)cluster_ctarank() : 0;
+  // row side, FP8 mode: the shard this CTA's k-range lies in
+  const int rshard = p.row ? (int)((int64_t)rank * p.tp / p.cs) : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < XS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
+    }
+    if (F8) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(smem_u32(&rfull[s]), 1);
+        mbar_init(smem_u32(&rempty[s]), SK_CONV_WARPS);  // one arrive per converter warp
+      }
     }
     for (int a = 0; a < p.acc_bufs; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
       mbar_init(smem_u32(&tempty[a]), 4);  // one arrive per epilogue warp
     }
     mbar_init(smem_u32(drain), 1);
+    if (F8) {
+      for (int c = 0; c < p.cstages; ++c) {
+        mbar_init(smem_u32(&cfull[c]), SK_GROUP_WARPS);  // one arrive per warp of its group
+        mbar_init(smem_u32(&cempty[c]), 1);
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -293,11 +400,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // The whole warp issues: lane 0 waits for the stage, arms its barrier and
-    // loads the X box; lane 1 + b loads weight box b of the tile.  Issuing the
-    // boxes from many lanes keeps the TMA unit fed.
-    int stage = 0;
+    // The whole warp issues: lane 0 waits for the stage(s), arms the barriers
+    // and loads the X box; lane 1 + b loads weight box b of the tile.  Issuing
+    // the boxes from many lanes keeps the TMA unit fed.  FP8 mode: the X box
+    // goes to the X ring, the codes to the raw ring, each with its barriers.
+    int stage = 0;      // X ring (bf16 mode: the one ring)
     uint32_t phase = 0;
+    int rs = 0;         // FP8: raw ring
+    uint32_t rphase = 0;
     bool ok = true;
     // X is re-read by every SM; the weights are streamed once.
     const uint64_t pol_x = l2_policy_evict_last();
@@ -309,46 +419,100 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         int64_t wrow = 0;     // first weight row of this lane's box in its shard buffer
         uint32_t woff = 0;    // its offset in the stage's B tile
         int wshard = 0;
+        constexpr int pitch = F8 ? SK_RAW_ROW_BYTES : SK_ROW_BYTES;  // bytes per loaded row
         if (mine) {
           const Piece& pc = tl.pc[piece];
           wrow = (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G + half * G : pc.loc) + r;
-          woff = (uint32_t)(pc.slot + half * tl.rows + r) * SK_ROW_BYTES;
+          woff = (uint32_t)(pc.slot + half * tl.rows + r) * pitch;
           wshard = pc.shard;
         }
-        uint32_t bytes = 0;
+        uint32_t wbytes = 0;  // weight (code) bytes of one stage
         if (lane == 0) {
-          bytes = (uint32_t)p.x_stage_bytes;
           for (int b = 0; b < tl.boxes; ++b) {
             int pi, hf, rr, hh;
-            if (tile_box(tl, swiglu, b, pi, hf, rr, hh)) bytes += (uint32_t)hh * SK_ROW_BYTES;
+            if (tile_box(tl, swiglu, b, pi, hf, rr, hh)) wbytes += (uint32_t)hh * pitch;
           }
         }
-        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-          const int rsh = p.row ? kb / p.kb_per_shard : 0;  // row side: shard of this k-block
-          const int kk = p.row ? kb - rsh * p.kb_per_shard : kb;
-          bool got = true;
-          if (lane == 0) got = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u);
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
-            if (lane == 0) report_error(p.err, kErrTimeoutProducer);
-            ok = false;
-            break;
+        if constexpr (F8) {
+          // one raw stage per SK_KPR k-blocks (fewer at the end of the range:
+          // a box reaching past the shard's K reads zeros that nobody uses),
+          // then the X boxes of those k-blocks, one per X stage
+          for (int kb = tl.kb0; kb < tl.kb1 && ok; kb += SK_KPR) {
+            const int nsub = tl.kb1 - kb < SK_KPR ? tl.kb1 - kb : SK_KPR;
+            const int rsh = p.row ? kb / p.kb_per_shard : 0;
+            const int kk = p.row ? kb - rsh * p.kb_per_shard : kb;
+            bool got = true;
+            if (lane == 0) got = mbar_wait_bounded(smem_u32(&rempty[rs]), rphase ^ 1u);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+              if (lane == 0) report_error(p.err, kErrTimeoutProducer);
+              ok = false;
+              break;
+            }
+            const uint32_t wb = smem_u32(&rfull[rs]);
+            if (lane == 0) {
+              mbar_arrive_expect_tx(wb, wbytes);
+            } else if (mine) {
+              const int sh = p.row ? rsh : wshard;
+              const CUtensorMap* map = (h == 64) ? &p.tmW64[sh] : &p.tmW16[sh];
+              tma_load_2d_hint(smem_u32(sR + (size_t)rs * p.raw_stage_bytes) + woff, map,
+                               kk * SK_BK, (int)wrow, wb, pol_w);
+            }
+            __syncwarp();
+            if (++rs == S) {
+              rs = 0;
+              rphase ^= 1u;
+            }
+            for (int j = 0; j < nsub; ++j) {
+              bool gx = true;
+              if (lane == 0) gx = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u);
+              gx = __shfl_sync(0xffffffffu, gx, 0);
+              if (!gx) {
+                if (lane == 0) report_error(p.err, kErrTimeoutProducer);
+                ok = false;
+                break;
+              }
+              if (lane == 0) {
+                const uint32_t fb = smem_u32(&full[stage]);
+                mbar_arrive_expect_tx(fb, (uint32_t)p.x_stage_bytes);
+                tma_load_2d_hint(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh],
+                                 (kk + j) * SK_BK, 0, fb, pol_x);
+              }
+              __syncwarp();
+              if (++stage == XS) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
           }
-          const uint32_t fb = smem_u32(&full[stage]);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(fb, bytes);
-            tma_load_2d_hint(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh], kk * SK_BK,
-                        0, fb, pol_x);
-          } else if (mine) {
-            const int sh = p.row ? rsh : wshard;
-            const CUtensorMap* map = (h == 64) ? &p.tmW64[sh] : &p.tmW16[sh];
-            tma_load_2d_hint(smem_u32(sW + (size_t)stage * p.w_stage_bytes) + woff, map, kk * SK_BK,
-                        (int)wrow, fb, pol_w);
-          }
-          __syncwarp();
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
+        } else {
+          for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+            const int rsh = p.row ? kb / p.kb_per_shard : 0;  // row side: shard of this k-block
+            const int kk = p.row ? kb - rsh * p.kb_per_shard : kb;
+            bool got = true;
+            if (lane == 0) got = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+              if (lane == 0) report_error(p.err, kErrTimeoutProducer);
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full[stage]);
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, (uint32_t)p.x_stage_bytes + wbytes);
+              tma_load_2d_hint(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh],
+                               kk * SK_BK, 0, fb, pol_x);
+            } else if (mine) {
+              const int sh = p.row ? rsh : wshard;
+              const CUtensorMap* map = (h == 64) ? &p.tmW64[sh] : &p.tmW16[sh];
+              tma_load_2d_hint(smem_u32(sW + (size_t)stage * p.w_stage_bytes) + woff, map,
+                               kk * SK_BK, (int)wrow, fb, pol_w);
+            }
+            __syncwarp();
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
@@ -361,6 +525,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int cst = 0;            // FP8 mode: bf16 buffer of this k-block
+    uint32_t cphase = 0;
     bool ok = true;
     SK_FOR_EACH_TILE(tl, {
       if (ok && !mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u)) {
@@ -376,14 +542,15 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
         const uint32_t idesc1 = idesc_bf16_f32(128, n1 > 0 ? n1 : 16);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
         for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase)) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase) ||
+              (F8 && !mbar_wait_bounded(smem_u32(&cfull[cst]), cphase))) {
             report_error(p.err, kErrTimeoutMma);
             ok = false;
             break;
           }
           tc_fence_after();
           const uint64_t adesc = sdesc_sw128(smem_u32(sX + (size_t)stage * p.x_stage_bytes));
-          const uint32_t wbase = smem_u32(sW + (size_t)stage * p.w_stage_bytes);
+          const uint32_t wbase = smem_u32(sW + (size_t)(F8 ? cst : stage) * p.w_stage_bytes);
           const uint64_t bdesc0 = sdesc_sw128(wbase);
           const uint64_t bdesc1 = sdesc_sw128(wbase + SK_BN * SK_ROW_BYTES);
 #pragma unroll
@@ -398,7 +565,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
                        idesc1, accum);
           }
           mma_commit(smem_u32(&empty[stage]));  // stage reusable once these MMAs finish
-          if (++stage == S) {
+          if (F8) {
+            mma_commit(smem_u32(&cempty[cst]));  // and the bf16 buffer
+            if (++cst == p.cstages) {
+              cst = 0;
+              cphase ^= 1u;
+            }
+          }
+          if (++stage == XS) {
             stage = 0;
             phase ^= 1u;
           }
@@ -413,7 +587,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     // every MMA this thread issued has completed before TMEM is released
     mma_commit(smem_u32(drain));
     if (!mbar_wait_bounded(smem_u32(drain), 0)) report_error(p.err, kErrTimeoutDrain);
-  } else if (warp >= SK_EPI_WARP0) {
+  } else if (warp >= SK_EPI_WARP0 && warp < SK_EPI_WARP0 + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                // TMEM lane quadrant this warp may access
     const int64_t t = q * 32 + lane;       // this thread's token
@@ -439,6 +613,13 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
           for (int j0 = 0; j0 < c; j0 += 8) {
             float v[8];
             tmem_ld8(taddr + (uint32_t)j0, v);
+            if (F8) {
+              // this CTA's partial belongs to shard rshard: its row scales
+              const float* sc = p.wscale[rshard] + tl.pc[0].loc + j0;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (j0 + j < c) v[j] *= __ldg(sc + j);
+            }
             if (t < p.M) {
               float4* dst = reinterpret_cast<float4*>(red + t * SK_RED_PITCH + j0);
               dst[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -450,14 +631,29 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
             const Piece& pc = tl.pc[i];
             const int64_t base = (p.row ? 0 : p.yoff[pc.shard]) + t * p.ldy;
             const float* bias = p.row ? p.bias[0] : (swiglu ? nullptr : p.bias[pc.shard]);
+            // FP8 mode: scales of the piece's (gate) rows; up rows G further
+            const float* sc = nullptr;
+            if (F8)
+              sc = p.wscale[p.row ? rshard : pc.shard] +
+                   (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G : pc.loc);
 #pragma unroll 1
             for (int j0 = 0; j0 < pc.c; j0 += 8) {
               float v[8];
               tmem_ld8(taddr + (uint32_t)(pc.slot + j0), v);
               const int valid = pc.c - j0 < 8 ? pc.c - j0 : 8;
+              if (F8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (j < valid) v[j] *= __ldg(sc + j0 + j);
+              }
               if (swiglu) {
                 float u[8];
                 tmem_ld8(taddr + (uint32_t)(tl.rows + pc.slot + j0), u);
+                if (F8) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    if (j < valid) u[j] *= __ldg(sc + G + j0 + j);
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = act_silu(v[j]) * u[j];
               } else {
@@ -486,6 +682,84 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     });
   }
 
+  if (F8 && warp >= SK_CONV_WARP0) {
+    // ------------------------------------------------------------ converters
+    // A raw stage holds SK_KPR k-blocks of each tile row (rows SK_RAW_ROW_BYTES
+    // apart); each k-block becomes one bf16 B tile in the 128-byte swizzled
+    // K-major layout the MMA's descriptor expects.  k-block n of the CTA's
+    // sequence is converted by group n mod 2 into buffer n mod 2.  Thread gt
+    // of a group owns 16-byte chunk c4 = gt mod 4 of a k-block (codes
+    // [16 c4, 16 c4 + 16)) in rows gt / 4, gt / 4 + SK_GROUP_THREADS / 4, ...;
+    // it writes them as bf16 chunks 2 c4 and 2 c4 + 1 of the row, each at
+    // chunk position c ^ (row mod 8).  Every converter warp releases each raw
+    // stage once, whether or not its group had a k-block in it.
+    const int cw = warp - SK_CONV_WARP0;
+    const int grp = cw / SK_GROUP_WARPS;
+    const int gt = (cw % SK_GROUP_WARPS) * 32 + lane;
+    const int row0 = gt >> 2, c4 = gt & 3, sw = row0 & 7;
+    constexpr int RSTEP = SK_GROUP_THREADS / 4;
+    const uint32_t src0 = (uint32_t)(row0 * SK_RAW_ROW_BYTES + c4 * 16);
+    const uint32_t dlo0 = (uint32_t)(row0 * SK_ROW_BYTES + (((2 * c4) ^ sw) << 4));
+    const uint32_t dhi0 = (uint32_t)(row0 * SK_ROW_BYTES + (((2 * c4 + 1) ^ sw) << 4));
+    uint8_t* const mybuf = sW + (size_t)grp * p.w_stage_bytes;
+    int rs = 0;
+    uint32_t rphase = 0, cphase = 0;
+    int64_t n = 0;  // k-blocks of the CTA's sequence before this raw stage
+    bool ok = true;
+    SK_FOR_EACH_TILE(tl, {
+      if (ok) {
+        const int nrows = swiglu ? 2 * tl.rows : tl.rows;
+        for (int kb = tl.kb0; kb < tl.kb1 && ok; kb += SK_KPR) {
+          const int nsub = tl.kb1 - kb < SK_KPR ? tl.kb1 - kb : SK_KPR;
+          bool got = mbar_wait_bounded(smem_u32(&rfull[rs]), rphase);
+          got = __all_sync(0xffffffffu, got);
+          if (!got) {
+            if (lane == 0) report_error(p.err, kErrTimeoutConvert);
+            ok = false;
+            break;
+          }
+          for (int j = 0; j < nsub; ++j) {
+            if ((int)((n + j) % SK_CONV_GROUPS) != grp) continue;
+            bool gc = mbar_wait_bounded(smem_u32(&cempty[grp]), cphase ^ 1u);
+            gc = __all_sync(0xffffffffu, gc);
+            if (!gc) {
+              if (lane == 0) report_error(p.err, kErrTimeoutConvert);
+              ok = false;
+              break;
+            }
+            const uint8_t* src = sR + (size_t)rs * p.raw_stage_bytes + src0 + j * SK_BK;
+            uint8_t* dst = mybuf;
+#pragma unroll 4
+            for (int r = row0; r < nrows; r += RSTEP) {
+              const uint4 q = *reinterpret_cast<const uint4*>(src);
+              uint4 lo, hi;
+              e4m3x4_to_bf16x4(q.x, lo.x, lo.y);
+              e4m3x4_to_bf16x4(q.y, lo.z, lo.w);
+              e4m3x4_to_bf16x4(q.z, hi.x, hi.y);
+              e4m3x4_to_bf16x4(q.w, hi.z, hi.w);
+              *reinterpret_cast<uint4*>(dst + dlo0) = lo;
+              *reinterpret_cast<uint4*>(dst + dhi0) = hi;
+              src += RSTEP * SK_RAW_ROW_BYTES;
+              dst += RSTEP * SK_ROW_BYTES;
+            }
+            fence_proxy_async_smem();  // the MMA reads these writes through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&cfull[grp]));
+            cphase ^= 1u;
+          }
+          if (!ok) break;
+          n += nsub;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&rempty[rs]));  // codes read: the raw stage is free
+          if (++rs == S) {
+            rs = 0;
+            rphase ^= 1u;
+          }
+        }
+      }
+    });
+  }
+
   __syncthreads();
   if (p.row && p.cs > 1) {
     // ---------------------------------------------------------- cluster reduction
@@ -503,7 +777,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     if (j_hi > j_lo) {
       const int span = j_hi - j_lo;
       const int64_t items = p.M * span;
-      for (int64_t it = threadIdx.x; it < items; it += SK_THREADS) {
+      for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
         const int64_t tok = it / span;
         const int j = j_lo + (int)(it - tok * span);
         const uint32_t off = (uint32_t)((tok * SK_RED_PITCH + j) * 4);
@@ -524,10 +798,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
 
 #undef SK_FOR_EACH_TILE
 
-}  // namespace
-
-tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
+template <bool F8>
+tp_status launch_skinny_mode(const LinearProblem& p, cudaStream_t stream) {
   if (p.xdt != TP_BF16 || p.M < 1 || p.M > kSkinnyMaxTokens) return TP_ERR_UNSUPPORTED;
+  if (F8 && p.row && p.tp > SK_MAX_CLUSTER) return TP_ERR_UNSUPPORTED;
   SkinnyParams sp{};
   sp.err = device_error_word();
   if (!sp.err) return TP_ERR_CUDA;
@@ -546,11 +820,22 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
   }
   for (int i = 0; i < p.tp; ++i) {
     const uint64_t rows = (uint64_t)(p.row ? p.w_rows : p.wr[i]);
-    if (!make_tma_map_bf16(&sp.tmW16[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 16) ||
-        !make_tma_map_bf16(&sp.tmW64[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 64))
-      return TP_ERR_CUDA;
+    bool ok;
+    if (F8) {  // e4m3 codes: one byte per weight
+      ok = make_tma_map_u8(&sp.tmW16[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)p.K,
+                           SK_RAW_ROW_BYTES, 16) &&
+           make_tma_map_u8(&sp.tmW64[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)p.K,
+                           SK_RAW_ROW_BYTES, 64);
+    } else {
+      ok = make_tma_map_bf16(&sp.tmW16[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 16) &&
+           make_tma_map_bf16(&sp.tmW64[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 64);
+    }
+    if (!ok) return TP_ERR_CUDA;
   }
-  for (int i = 0; i < TP_MAX_TP; ++i) sp.bias[i] = p.bias[i];
+  for (int i = 0; i < TP_MAX_TP; ++i) {
+    sp.bias[i] = p.bias[i];
+    sp.wscale[i] = F8 ? p.wscale[i] : nullptr;
+  }
   sp.Y = p.Y;
   sp.ldy = p.ldy;
   for (int i = 0; i <= p.tp; ++i) sp.fo[i] = p.fo[i];
@@ -575,6 +860,14 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
     const int64_t tiles = (p.n_out + SK_BN - 1) / SK_BN;
     int64_t cs = std::max<int64_t>(1, std::min<int64_t>(SK_MAX_CLUSTER, sms / tiles));
     cs = std::min<int64_t>(cs, sp.kb_total);
+    if (F8) {
+      // Each CTA's k-range must lie inside one shard (its partial is scaled
+      // by that shard's row scales): tp x j CTAs, j per shard.
+      const int64_t j = std::max<int64_t>(
+          1, std::min<int64_t>({(int64_t)SK_MAX_CLUSTER / p.tp, sms / (tiles * p.tp),
+                                (int64_t)sp.kb_per_shard}));
+      cs = p.tp * j;
+    }
     if (tiles * cs > INT32_MAX) return TP_ERR_BAD_SHAPE;
     sp.cs = (int)cs;
     grid = (int)(tiles * cs);
@@ -589,35 +882,45 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
   if (!p.row) {
     const int64_t units = (sp.feat_total + SK_GRAIN - 1) / SK_GRAIN;
     const int64_t max_range = (units + grid - 1) / grid * SK_GRAIN;
-    sp.tile_cap = (int)std::min<int64_t>(SK_BN, max_range);
+    // FP8 mode: at most 256 rows (gate + up) per tile
+    const int64_t cap = (F8 && swiglu) ? SK_BN / 2 : SK_BN;
+    sp.tile_cap = (int)std::min<int64_t>(cap, max_range);
     tile_rows = swiglu ? 2 * sp.tile_cap : sp.tile_cap;
   }
   sp.w_stage_bytes = tile_rows * SK_ROW_BYTES;
+  sp.raw_stage_bytes = F8 ? tile_rows * SK_RAW_ROW_BYTES : 0;
+  sp.cstages = F8 ? SK_CSTAGES : 0;
   sp.acc_stride = (tile_rows + 31) / 32 * 32;
   sp.acc_bufs = (SK_ACC_BUFS * sp.acc_stride <= SK_TMEM_COLS) ? SK_ACC_BUFS : 1;
   const int avail = SK_SMEM_MAX - 1024 - SK_BAR_BYTES;
-  const int stages = std::min(SK_MAX_STAGES, avail / (sp.x_stage_bytes + sp.w_stage_bytes));
+  // bf16: a stage is the X box and the weight rows.  FP8: a stage is the raw
+  // codes; the X ring (about 32 KB) and the bf16 buffers are fixed.
+  sp.xstages = F8 ? std::max(2, std::min(SK_MAX_STAGES, 32768 / sp.x_stage_bytes)) : 0;
+  const int per_stage = F8 ? sp.raw_stage_bytes : sp.x_stage_bytes + sp.w_stage_bytes;
+  const int fixed = F8 ? sp.xstages * sp.x_stage_bytes + sp.cstages * sp.w_stage_bytes : 0;
+  const int stages = std::min(SK_MAX_STAGES, (avail - fixed) / per_stage);
   if (stages < 2) return TP_ERR_UNSUPPORTED;
   sp.stages = stages;
-  const int ring = stages * (sp.x_stage_bytes + sp.w_stage_bytes);
+  const int ring = stages * per_stage + fixed;
+  const int x_ring_stages = F8 ? sp.xstages : stages;
   // The MMA reads a full 128-row A tile from each X stage: the read past the
-  // last X stage runs into the weight stages, which must be there.  (It reads
-  // only the tile's rows from a weight stage.)  The row side's reduction
-  // buffer reuses the ring.
-  if ((stages - 1) * sp.x_stage_bytes + SK_A_BYTES > ring) return TP_ERR_UNSUPPORTED;
+  // last X stage runs into the stages after the X ring (weights, or codes in
+  // FP8 mode), which must be there.  The row side's reduction buffer reuses
+  // the ring.
+  if ((x_ring_stages - 1) * sp.x_stage_bytes + SK_A_BYTES > ring) return TP_ERR_UNSUPPORTED;
   if (p.row && sp.cs > 1 && (int64_t)xrows * SK_RED_PITCH * 4 > ring) return TP_ERR_UNSUPPORTED;
   const int smem = 1024 + ring + SK_BAR_BYTES;
 
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SK_SMEM_MAX);
+    attr_err = cudaFuncSetAttribute(skinny_kernel<F8>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_MAX);
   });
   if (attr_err != cudaSuccess) return TP_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(SK_THREADS);
+  cfg.blockDim = dim3(F8 ? SK_THREADS_F8 : SK_THREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -627,8 +930,14 @@ tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, skinny_kernel, sp) != cudaSuccess) return TP_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, skinny_kernel<F8>, sp) != cudaSuccess) return TP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // namespace
+
+tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
+  return p.fp8 ? launch_skinny_mode<true>(p, stream) : launch_skinny_mode<false>(p, stream);
 }
 
 }  // namespace tpla

@@ -21,6 +21,7 @@ enum : uint32_t {
   kErrTimeoutEpilogue = 1u << 2,
   kErrTimeoutDrain = 1u << 3,
   kErrSelftest = 1u << 4,
+  kErrTimeoutConvert = 1u << 5,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

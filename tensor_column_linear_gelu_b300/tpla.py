@@ -34,7 +34,7 @@ TP_SPLIT_COLUMN, TP_SPLIT_ROW, TP_SPLIT_QKV_HEADS, TP_SPLIT_GATE_UP = 0, 1, 2, 3
 TP_MAX_TP = 16
 TP_GATE_UP_GROUP = 128
 TP_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
-TP_FP8_MAX_TOKENS = 8
+TP_FP8_MAX_TOKENS = 128
 
 ACTS = {"none": TP_ACT_NONE, "gelu": TP_ACT_GELU_ERF, "swiglu": TP_ACT_SWIGLU}
 SPLITS = {"column": TP_SPLIT_COLUMN, "row": TP_SPLIT_ROW, "qkv_heads": TP_SPLIT_QKV_HEADS,

@@ -164,7 +164,7 @@ rec("fp8_quant_null", QZ(4, 64, A, None, A, None))
 rec("fp8_quant_cols0", QZ(4, 0, A, A, A, None))
 CF = L.column_parallel_linear_fp8
 rec("fp8_col_f32_x", CF(2, 4, 64, 64, A, 64, F32, w2, w2, None, 0, A, 64, F32, None))
-rec("fp8_col_too_many_tokens", CF(2, 9, 64, 64, A, 64, BF, w2, w2, None, 0, A, 64, BF, None))
+rec("fp8_col_too_many_tokens", CF(2, 129, 64, 64, A, 64, BF, w2, w2, None, 0, A, 64, BF, None))
 rec("fp8_col_null_scales", CF(2, 4, 64, 64, A, 64, BF, w2, None, None, 0, A, 64, BF, None))
 rec("fp8_col_K_not16", CF(2, 4, 72, 64, A, 72, BF, w2, w2, None, 0, A, 64, BF, None))
 rec("fp8_col_swiglu_bias", CF(2, 4, 64, 64, A, 64, BF, w2, w2, w2, 2, A, 64, BF, None))
@@ -174,7 +174,7 @@ rec("fp8_row_notdiv", RF(3, 4, 64, 64, A, 64, BF, arr(A, A, A), arr(A, A, A), No
 rec("fp8_row_M0", RF(2, 0, 64, 64, None, 64, BF, None, None, None, None, 64, BF, None))
 MF = L.tp_mlp_block_fp8
 rec("fp8_mlp_null_h", MF(2, 4, 64, 128, 2, A, w2, w2, None, w2, w2, None, None, A, BF, None))
-rec("fp8_mlp_too_many", MF(2, 16, 64, 128, 2, A, w2, w2, None, w2, w2, None, A, A, BF, None))
+rec("fp8_mlp_too_many", MF(2, 129, 64, 128, 2, A, w2, w2, None, w2, w2, None, A, A, BF, None))
 json.dump(res, sys.stdout)
 '''
 

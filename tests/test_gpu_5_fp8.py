@@ -9,6 +9,10 @@
   weights itself; nothing it uses comes from the GPU.  Tolerance: the bf16
   one (5e-3 x RMS, fp32 output); the FFN's h (bf16) within half a bf16 ulp.
 * The FP8 column split is bit-identical to tp = 1, as the bf16 one is.
+* Both kernels are covered: the FP8 GEMV (one or two tokens) and the tensor-
+  core decode kernel in its FP8 mode (3..128 tokens), which widens the codes
+  to bf16 in shared memory: every one of the 254 finite e4m3 codes goes
+  through each kernel once and must come out as its exact value.
 """
 import numpy as np
 import pytest
@@ -48,7 +52,9 @@ def test_quantizer_matches_oracle_bitwise(orc):
 # M, K, N, tp, act, bias
 COLUMN_CASES = [(1, 256, 96, 2, "none", True), (2, 512, 384, 4, "gelu", True),
                 (5, 1024, 600, 3, "gelu", False), (8, 256, 520, 4, "swiglu", False),
-                (1, 4096, 2048, 8, "swiglu", False)]
+                (1, 4096, 2048, 8, "swiglu", False), (3, 320, 48, 1, "none", False),
+                (16, 1024, 1000, 4, "gelu", True), (64, 512, 2304, 2, "swiglu", False),
+                (128, 256, 384, 3, "none", True), (33, 2048, 4096, 8, "swiglu", False)]
 
 
 @pytest.mark.parametrize("M,K,N,tp,act,bias", COLUMN_CASES)
@@ -76,8 +82,10 @@ def test_fp8_column_parallel(orc, M, K, N, tp, act, bias):
     assert tpla.tp_device_status() == tpla.TP_OK
 
 
-# M, K, N, tp, bias
-ROW_CASES = [(1, 512, 64, 2, True), (3, 1536, 200, 3, False), (8, 4096, 256, 8, True)]
+# M, K, N, tp, bias  (tp = 16 row calls with M > 2 take the GEMV)
+ROW_CASES = [(1, 512, 64, 2, True), (3, 1536, 200, 3, False), (8, 4096, 256, 8, True),
+             (16, 1024, 520, 4, True), (64, 2048, 1024, 2, False), (128, 512, 300, 1, True),
+             (5, 4096, 96, 16, True), (40, 3072, 768, 6, False)]
 
 
 @pytest.mark.parametrize("M,K,N,tp,bias", ROW_CASES)
@@ -96,7 +104,7 @@ def test_fp8_row_parallel(orc, M, K, N, tp, bias):
     assert tpla.tp_device_status() == tpla.TP_OK
 
 
-@pytest.mark.parametrize("M,tp", [(1, 4), (2, 4), (8, 2)])
+@pytest.mark.parametrize("M,tp", [(1, 4), (2, 4), (8, 2), (3, 4), (64, 8)])
 def test_fp8_ffn_block(orc, M, tp):
     d, dff = 1024, 4096
     f = inputs.ffn(seed=40 + M, M=M, d_model=d, d_ff=dff, act="swiglu", bias=False, device=DEV)
@@ -133,3 +141,35 @@ def test_fp8_quantizer_full_size_sampled_rows(orc):
     q_ref, s_ref = orc.quantize_rows_fp8(w1[1][rows])
     assert np.array_equal(S[rows].cpu().numpy(), s_ref)
     assert np.array_equal(codes_to_float(Q[rows]), q_ref)
+
+
+def e4m3_table() -> np.ndarray:
+    """Value of every e4m3 code (NaN for the two NaN codes), decoded by torch's
+    CPU float8 type."""
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_every_e4m3_code_exact(orc, M):
+    """W[n, k] = the value of code (n + k) mod 256 (NaN codes -> +-448), so every
+    row holds 448, its scale is 1 and its codes are the table itself; token m is
+    one-hot at column m, so Y[m, n] is the value of code (n + m) mod 256."""
+    vals = e4m3_table()
+    vals[0x7F], vals[0xFF] = 448.0, -448.0
+    N = K = 256
+    codes = (np.arange(N)[:, None] + np.arange(K)[None, :]) % 256
+    W = torch.from_numpy(vals[codes]).to(torch.bfloat16).to(DEV)
+    X = torch.zeros(M, K, dtype=torch.bfloat16, device=DEV)
+    X[torch.arange(M), torch.arange(M)] = 1.0
+    Q, S = tpla.tp_quantize_fp8(W)
+    torch.cuda.synchronize()
+    assert torch.all(S == 1.0)
+    want = torch.from_numpy(codes.astype(np.uint8))
+    want[want == 0x7F], want[want == 0xFF] = 0x7E, 0xFE
+    assert torch.equal(Q.cpu(), want)
+    y = tpla.column_parallel_linear_fp8(1, X, [Q], [S], None, "none", out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    exact = vals[codes[:, :M].T]          # [M, N]
+    assert np.array_equal(y.cpu().numpy(), exact)
+    q_ref, s_ref = orc.quantize_rows_fp8(W)
+    assert np.array_equal(orc.column_parallel_fp8(1, X, q_ref, s_ref), exact)
