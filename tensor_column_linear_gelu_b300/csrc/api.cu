@@ -74,14 +74,17 @@ tp_status check_bias_array(const float* const* b, int tp) {
 //   bf16, kGemvMaxTokens < M <= kSkinnyMaxTokens  tcgen05 decode kernel
 //   bf16, M > kSkinnyMaxTokens                    tcgen05 prefill GEMM
 //   FP8 weights, M <= kGemvMaxTokens              FP8 weight-streaming GEMV
+//   FP8 weights, M <= kFp8TmemMaxTokens           tcgen05 FP8 decode kernel, weights in TMEM
 //   FP8 weights, larger M                         tcgen05 decode kernel, FP8 mode
-// (FP8 row-parallel calls with tp above the decode kernel's largest cluster
-// also take the FP8 GEMV: its CTAs must each hold one shard's k-range.)
+// (FP8 row-parallel calls with tp above the decode kernels' largest cluster
+// also take the FP8 GEMV: their CTAs must each hold one shard's k-range.)
 tp_status run(const LinearProblem& p, cudaStream_t s) {
   if (p.M == 0) return TP_OK;
   if (p.fp8) {
-    if (p.M > kGemvMaxTokens && !(p.row && p.tp > kSkinnyMaxCluster)) return launch_skinny(p, s);
-    return launch_gemv_fp8(p, s);
+    if (p.M <= kGemvMaxTokens || (p.row && p.tp > kSkinnyMaxCluster))
+      return launch_gemv_fp8(p, s);
+    if (p.M <= kFp8TmemMaxTokens) return launch_decode_fp8(p, s);
+    return launch_skinny(p, s);
   }
   if (p.xdt == TP_BF16 && p.M > kGemvMaxTokens) {
     if (p.M <= kSkinnyMaxTokens) return launch_skinny(p, s);

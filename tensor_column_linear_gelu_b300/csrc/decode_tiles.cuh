@@ -1,0 +1,179 @@
+// decode_tiles.cuh -- pieces shared by the two tcgen05 decode kernels
+// (skinny.cu: weights as the MMA's N operand from shared memory;
+// decode_fp8.cu: e4m3 weights widened into tensor memory as its A operand):
+// the e4m3 -> bf16 widening, and the tiling of a CTA's outputs into pieces
+// of consecutive features at 16-row slots.  The tiling functions take any
+// parameter struct with the fields they read (tile_cap, act, tp, fo,
+// kb_total, feat_total, cs).
+#pragma once
+
+#include <cstdint>
+
+#include "tpla.h"
+
+namespace tpla {
+namespace decode {
+
+constexpr int SK_GRAIN = 16;                // features per balance unit (column side)
+constexpr int SK_MAX_BOXES = 31;            // weight boxes per stage (one per producer lane)
+constexpr int SK_BN = 256;                  // outputs per row-side tile
+constexpr int64_t G = TP_GATE_UP_GROUP;
+static_assert(2 * G == SK_BN, "a gate/up group's rows fill one 256-row tile");
+
+__device__ __forceinline__ int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Byte permute (PTX prmt, default mode): result byte i is byte (sel_i & 7)
+// of {a, 0}, or that byte's sign bit replicated when sel_i & 8.
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
+  return r;
+}
+
+// Two e4m3 codes to two bf16 values, exactly.  Each 16-bit lane of w holds a
+// code in its low byte and the code's sign replicated through its high byte:
+// s s s s s s s s | s e e e e m m m.  Shifted left by 4 (the low lane's top
+// nibble spills into bits 0-3 of the high lane, which the mask clears) and
+// masked, a lane keeps the sign at bit 15 and the code's exponent and
+// mantissa at bits 7..10 and 4..6: read as bf16 that is the e4m3 value times
+// 2^-120 (bf16 exponent bias 127 against e4m3's 7; a subnormal code gives the
+// matching subnormal bf16).  One bf16x2 multiply by 2^120 (0x7B80) restores
+// the value; no step rounds.
+__device__ __forceinline__ uint32_t e4m3_lanes_to_bf16x2(uint32_t w) {
+  const uint32_t bits = (w << 4) & 0x87F087F0u;
+  uint32_t out;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(bits), "r"(0x7B807B80u));
+  return out;
+}
+
+// Four e4m3 codes (code k in byte k of q) to four bf16 values: codes 0, 1 in
+// lo (low half first), codes 2, 3 in hi.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t q, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3_lanes_to_bf16x2(prmt_b32(q, 0x9180u));  // bytes: q0, sign(q0), q1, sign(q1)
+  hi = e4m3_lanes_to_bf16x2(prmt_b32(q, 0xB3A2u));  // bytes: q2, sign(q2), q3, sign(q3)
+}
+
+constexpr int SK_MAX_PIECES = 8;
+
+// One B tile's worth of work: up to SK_MAX_PIECES pieces of consecutive
+// output features, each at a 16-row slot of the tile, and the k-blocks of its
+// K loop.
+struct Piece {
+  int shard;    // column: shard of the piece; row: unused (per k-block)
+  int64_t loc;  // column: first shard-local feature; row: first output
+  int c;        // features (outputs) in the piece
+  int slot;     // first row of the piece in the B tile (a multiple of 16)
+};
+struct Tile {
+  int n;        // pieces
+  int rows;     // slot rows used (a multiple of 16)
+  int boxes;    // weight TMA boxes per stage
+  int kb0, kb1; // k-blocks [kb0, kb1) of the tile's K loop
+  Piece pc[SK_MAX_PIECES];
+};
+
+// Weight boxes of a piece of c rows: whole 64-row boxes, then 16-row boxes.
+__device__ __forceinline__ int piece_boxes(int c) { return c / 64 + ((c % 64) + 15) / 16; }
+
+// Box `want` (0-based) of a tile, in the order pieces, then gate/up halves,
+// then rows: which piece and half, its first row within the piece, and its
+// height.  Returns false when the tile has fewer boxes.
+__device__ __forceinline__ bool tile_box(const Tile& t, bool swiglu, int want, int& piece,
+                                         int& half, int& r, int& h) {
+  int b = 0;
+  for (int i = 0; i < t.n; ++i)
+    for (int hf = 0; hf < (swiglu ? 2 : 1); ++hf) {
+      const int c = t.pc[i].c;
+      for (int rr = 0; rr < c; ++b) {
+        const int hh = (rr + 64 <= c) ? 64 : 16;
+        if (b == want) {
+          piece = i;
+          half = hf;
+          r = rr;
+          h = hh;
+          return true;
+        }
+        rr += hh;
+      }
+    }
+  return false;
+}
+
+// Column side: the tile starting at global feature f of a range ending at f1;
+// advances f past the features it takes.
+template <class P>
+__device__ __forceinline__ Tile column_tile(const P& p, int64_t& f, int64_t f1) {
+  const bool swiglu = p.act == TP_ACT_SWIGLU;
+  const int cap = p.tile_cap;  // slot rows per tile (features for SwiGLU)
+  Tile t;
+  t.n = 0;
+  t.rows = 0;
+  t.kb0 = 0;
+  t.kb1 = p.kb_total;
+  t.boxes = 0;
+  while (f < f1 && t.n < SK_MAX_PIECES && t.rows < cap) {
+    int sh = 0;
+    while (sh + 1 < p.tp && p.fo[sh + 1] <= f) ++sh;
+    const int64_t loc = f - p.fo[sh];
+    int64_t lim = imin(f1 - f, p.fo[sh + 1] - f);
+    if (swiglu) lim = imin(lim, G - loc % G);
+    const int c = (int)imin(lim, cap - t.rows);
+    const int nb = piece_boxes(c) * (swiglu ? 2 : 1);
+    if (t.n > 0 && t.boxes + nb > SK_MAX_BOXES) break;
+    t.pc[t.n].shard = (int)sh;
+    t.pc[t.n].loc = loc;
+    t.pc[t.n].c = c;
+    t.pc[t.n].slot = t.rows;
+    ++t.n;
+    t.boxes += nb;
+    t.rows += (c + 15) / 16 * 16;
+    f += c;
+  }
+  return t;
+}
+
+// Column side: this CTA's feature range [f0, f1), balanced in units of 8.
+template <class P>
+__device__ __forceinline__ void column_range(const P& p, int64_t& f0, int64_t& f1) {
+  const int64_t units = (p.feat_total + SK_GRAIN - 1) / SK_GRAIN;
+  const int64_t u0 = (int64_t)blockIdx.x * units / gridDim.x;
+  const int64_t u1 = ((int64_t)blockIdx.x + 1) * units / gridDim.x;
+  f0 = imin(u0 * SK_GRAIN, p.feat_total);
+  f1 = imin(u1 * SK_GRAIN, p.feat_total);
+}
+
+// Row side: the one tile of this CTA -- its cluster's 256 outputs and its
+// rank's share of the k-blocks.
+template <class P>
+__device__ __forceinline__ Tile row_tile(const P& p, int rank) {
+  Tile t;
+  const int64_t tile = blockIdx.x / p.cs;
+  t.n = 1;
+  t.pc[0].shard = 0;
+  t.pc[0].loc = tile * SK_BN;
+  t.pc[0].c = (int)imin(SK_BN, p.feat_total - t.pc[0].loc);
+  t.pc[0].slot = 0;
+  t.rows = (t.pc[0].c + 15) / 16 * 16;
+  t.boxes = piece_boxes(t.pc[0].c);
+  t.kb0 = (int)((int64_t)rank * p.kb_total / p.cs);
+  t.kb1 = (int)((int64_t)(rank + 1) * p.kb_total / p.cs);
+  return t;
+}
+
+// Loop over this CTA's tiles: the column side walks its feature range, the
+// row side has one tile.
+#define SK_FOR_EACH_TILE(tl, ...)                                     \
+  do {                                                                \
+    if (p.row) {                                                      \
+      const Tile tl = row_tile(p, rank);                              \
+      __VA_ARGS__                                                     \
+    } else {                                                          \
+      for (int64_t f_ = f0; f_ < f1;) {                               \
+        const Tile tl = column_tile(p, f_, f1);                       \
+        __VA_ARGS__                                                   \
+      }                                                               \
+    }                                                                 \
+  } while (0)
+
+}  // namespace decode
+}  // namespace tpla

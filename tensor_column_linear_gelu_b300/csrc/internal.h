@@ -78,16 +78,21 @@ bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint6
                        uint64_t ld_bytes, uint32_t box_rows);
 
 // 2-D byte tensor map (e4m3 codes): boxes of box_inner bytes (a multiple of
-// 16, at most 256) x box_rows rows, no swizzle (rows land box_inner bytes
-// apart), out-of-range bytes read as zero.
+// 16, at most 256; exactly 128 with swizzle128) x box_rows rows, rows landing
+// box_inner bytes apart, either plain or with the 128-byte swizzle (16-byte
+// chunk c of row r at chunk c ^ (r mod 8)); out-of-range bytes read as zero.
 bool make_tma_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                     uint64_t ld_bytes, uint32_t box_inner, uint32_t box_rows);
+                     uint64_t ld_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 
 // FP8 (e4m3) weights, bf16 activations, at most kFp8MaxTokens tokens: the
 // per-row quantizer; the weight-streaming FP8 GEMV (M <= kGemvMaxTokens, and
-// row-parallel calls whose tp exceeds the largest cluster); otherwise the
-// decode kernel in its FP8 mode (launch_skinny with p.fp8).
+// row-parallel calls whose tp exceeds the largest cluster); the FP8 decode
+// kernel with the widened weights in tensor memory (M <= kFp8TmemMaxTokens);
+// above that the shared-memory decode kernel in its FP8 mode (launch_skinny
+// with p.fp8).
 constexpr int64_t kFp8MaxTokens = kSkinnyMaxTokens;
+constexpr int64_t kFp8TmemMaxTokens = 64;
+tp_status launch_decode_fp8(const LinearProblem& p, cudaStream_t stream);
 tp_status launch_quantize_fp8(const void* W, int64_t rows, int64_t cols, void* Q, float* S,
                               cudaStream_t stream);
 tp_status launch_gemv_fp8(const LinearProblem& p, cudaStream_t stream);

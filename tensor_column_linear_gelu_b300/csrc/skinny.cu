@@ -62,11 +62,13 @@
 //               reduction.
 //   warps 6-21  FP8 mode only: the converters (below).
 //
-// FP8 mode (e4m3 weight codes + one fp32 scale per weight row).  The codes
+// FP8 mode (e4m3 weight codes + one fp32 scale per weight row; used above
+// the token count of the FP8 kernel in decode_fp8.cu, which widens the codes
+// into tensor memory instead of shared memory).  The codes
 // are streamed at one byte per weight -- half the bytes of bf16, which is the
 // point for a call bound by weight bytes -- and widened on chip:
-//   * the producer loads the same boxes as in bf16 mode, 64 codes wide, into
-//     a ring of raw stages (rows 64 bytes apart, no swizzle);
+//   * the producer loads the same rows as in bf16 mode, SK_KPR k-blocks of
+//     codes wide (128 bytes), into a ring of raw stages (no swizzle);
 //   * sixteen converter warps (two groups taking alternate k-blocks) turn
 //     each k-block of a raw stage into a bf16 B tile laid out
 //     exactly as a 128-byte-swizzled TMA load would have left it (16-byte
@@ -95,12 +97,15 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_tiles.cuh"
 #include "internal.h"
 #include "sync.cuh"
 #include "tc_ptx.cuh"
 
 namespace tpla {
 namespace {
+
+using namespace decode;
 
 constexpr int SK_THREADS = 192;
 constexpr int SK_EPI_WARP0 = 2;
@@ -130,19 +135,14 @@ constexpr int SK_CSTAGES = 2;               // FP8 mode: bf16 B-tile buffers, on
 constexpr int SK_MAX_CSTAGES = 4;
 static_assert(SK_CSTAGES == SK_CONV_GROUPS, "k-block n uses buffer n mod 2, converted by group n mod 2");
 constexpr int SK_A_BYTES = 128 * SK_ROW_BYTES;  // the A tile one MMA reads (128 rows)
-constexpr int SK_BN = 256;                  // weight rows per MMA (its N, at most)
 constexpr int SK_MAX_STAGES = 16;
 constexpr int SK_ACC_BUFS = 2;              // accumulator buffers, when two fit in TMEM
 constexpr int SK_TMEM_COLS = 512;
-constexpr int SK_GRAIN = 16;                // features per balance unit (column side)
-constexpr int SK_MAX_BOXES = 31;            // weight boxes per stage (one per producer lane)
 constexpr int SK_MAX_CLUSTER = kSkinnyMaxCluster;
 constexpr int SK_RED_PITCH = SK_BN + 4;     // floats per token row of a reduction buffer
 constexpr int SK_NUM_BARS = 4 * SK_MAX_STAGES + 2 * SK_ACC_BUFS + 1 + 2 * SK_MAX_CSTAGES;
 constexpr int SK_BAR_BYTES = SK_NUM_BARS * 8 + 16;
 constexpr int SK_SMEM_MAX = 232448;         // dynamic shared memory per CTA (227 KB)
-constexpr int64_t G = TP_GATE_UP_GROUP;
-static_assert(2 * G == SK_BN, "a gate/up group's rows fill one MMA");
 
 struct SkinnyParams {
   CUtensorMap tmX[TP_MAX_TP];    // column: [0] = X; row: X_i.  Box {64, xrows}.
@@ -167,158 +167,6 @@ struct SkinnyParams {
   int kb_per_shard, kb_total;
   int cs;                        // row side: CTAs per cluster splitting K
 };
-
-__device__ __forceinline__ int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
-
-// Byte permute (PTX prmt, default mode): result byte i is byte (sel_i & 7)
-// of {a, 0}, or that byte's sign bit replicated when sel_i & 8.
-__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
-  return r;
-}
-
-// Two e4m3 codes to two bf16 values, exactly.  Each 16-bit lane of w holds a
-// code in its low byte and the code's sign replicated through its high byte:
-// s s s s s s s s | s e e e e m m m.  Shifted left by 4 (the low lane's top
-// nibble spills into bits 0-3 of the high lane, which the mask clears) and
-// masked, a lane keeps the sign at bit 15 and the code's exponent and
-// mantissa at bits 7..10 and 4..6: read as bf16 that is the e4m3 value times
-// 2^-120 (bf16 exponent bias 127 against e4m3's 7; a subnormal code gives the
-// matching subnormal bf16).  One bf16x2 multiply by 2^120 (0x7B80) restores
-// the value; no step rounds.
-__device__ __forceinline__ uint32_t e4m3_lanes_to_bf16x2(uint32_t w) {
-  const uint32_t bits = (w << 4) & 0x87F087F0u;
-  uint32_t out;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(bits), "r"(0x7B807B80u));
-  return out;
-}
-
-// Four e4m3 codes (code k in byte k of q) to four bf16 values: codes 0, 1 in
-// lo (low half first), codes 2, 3 in hi.
-__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t q, uint32_t& lo, uint32_t& hi) {
-  lo = e4m3_lanes_to_bf16x2(prmt_b32(q, 0x9180u));  // bytes: q0, sign(q0), q1, sign(q1)
-  hi = e4m3_lanes_to_bf16x2(prmt_b32(q, 0xB3A2u));  // bytes: q2, sign(q2), q3, sign(q3)
-}
-
-constexpr int SK_MAX_PIECES = 8;
-
-// One B tile's worth of work: up to SK_MAX_PIECES pieces of consecutive
-// output features, each at a 16-row slot of the tile, and the k-blocks of its
-// K loop.
-struct Piece {
-  int shard;    // column: shard of the piece; row: unused (per k-block)
-  int64_t loc;  // column: first shard-local feature; row: first output
-  int c;        // features (outputs) in the piece
-  int slot;     // first row of the piece in the B tile (a multiple of 16)
-};
-struct Tile {
-  int n;        // pieces
-  int rows;     // slot rows used (a multiple of 16)
-  int boxes;    // weight TMA boxes per stage
-  int kb0, kb1; // k-blocks [kb0, kb1) of the tile's K loop
-  Piece pc[SK_MAX_PIECES];
-};
-
-// Weight boxes of a piece of c rows: whole 64-row boxes, then 16-row boxes.
-__device__ __forceinline__ int piece_boxes(int c) { return c / 64 + ((c % 64) + 15) / 16; }
-
-// Box `want` (0-based) of a tile, in the order pieces, then gate/up halves,
-// then rows: which piece and half, its first row within the piece, and its
-// height.  Returns false when the tile has fewer boxes.
-__device__ __forceinline__ bool tile_box(const Tile& t, bool swiglu, int want, int& piece,
-                                         int& half, int& r, int& h) {
-  int b = 0;
-  for (int i = 0; i < t.n; ++i)
-    for (int hf = 0; hf < (swiglu ? 2 : 1); ++hf) {
-      const int c = t.pc[i].c;
-      for (int rr = 0; rr < c; ++b) {
-        const int hh = (rr + 64 <= c) ? 64 : 16;
-        if (b == want) {
-          piece = i;
-          half = hf;
-          r = rr;
-          h = hh;
-          return true;
-        }
-        rr += hh;
-      }
-    }
-  return false;
-}
-
-// Column side: the tile starting at global feature f of a range ending at f1;
-// advances f past the features it takes.
-__device__ __forceinline__ Tile column_tile(const SkinnyParams& p, int64_t& f, int64_t f1) {
-  const bool swiglu = p.act == TP_ACT_SWIGLU;
-  const int cap = p.tile_cap;  // slot rows per tile (features for SwiGLU)
-  Tile t;
-  t.n = 0;
-  t.rows = 0;
-  t.kb0 = 0;
-  t.kb1 = p.kb_total;
-  t.boxes = 0;
-  while (f < f1 && t.n < SK_MAX_PIECES && t.rows < cap) {
-    int sh = 0;
-    while (sh + 1 < p.tp && p.fo[sh + 1] <= f) ++sh;
-    const int64_t loc = f - p.fo[sh];
-    int64_t lim = imin(f1 - f, p.fo[sh + 1] - f);
-    if (swiglu) lim = imin(lim, G - loc % G);
-    const int c = (int)imin(lim, cap - t.rows);
-    const int nb = piece_boxes(c) * (swiglu ? 2 : 1);
-    if (t.n > 0 && t.boxes + nb > SK_MAX_BOXES) break;
-    t.pc[t.n].shard = (int)sh;
-    t.pc[t.n].loc = loc;
-    t.pc[t.n].c = c;
-    t.pc[t.n].slot = t.rows;
-    ++t.n;
-    t.boxes += nb;
-    t.rows += (c + 15) / 16 * 16;
-    f += c;
-  }
-  return t;
-}
-
-// Column side: this CTA's feature range [f0, f1), balanced in units of 8.
-__device__ __forceinline__ void column_range(const SkinnyParams& p, int64_t& f0, int64_t& f1) {
-  const int64_t units = (p.feat_total + SK_GRAIN - 1) / SK_GRAIN;
-  const int64_t u0 = (int64_t)blockIdx.x * units / gridDim.x;
-  const int64_t u1 = ((int64_t)blockIdx.x + 1) * units / gridDim.x;
-  f0 = imin(u0 * SK_GRAIN, p.feat_total);
-  f1 = imin(u1 * SK_GRAIN, p.feat_total);
-}
-
-// Row side: the one tile of this CTA -- its cluster's 256 outputs and its
-// rank's share of the k-blocks.
-__device__ __forceinline__ Tile row_tile(const SkinnyParams& p, int rank) {
-  Tile t;
-  const int64_t tile = blockIdx.x / p.cs;
-  t.n = 1;
-  t.pc[0].shard = 0;
-  t.pc[0].loc = tile * SK_BN;
-  t.pc[0].c = (int)imin(SK_BN, p.feat_total - t.pc[0].loc);
-  t.pc[0].slot = 0;
-  t.rows = (t.pc[0].c + 15) / 16 * 16;
-  t.boxes = piece_boxes(t.pc[0].c);
-  t.kb0 = (int)((int64_t)rank * p.kb_total / p.cs);
-  t.kb1 = (int)((int64_t)(rank + 1) * p.kb_total / p.cs);
-  return t;
-}
-
-// Loop over this CTA's tiles: the column side walks its feature range, the
-// row side has one tile.
-#define SK_FOR_EACH_TILE(tl, ...)                                     \
-  do {                                                                \
-    if (p.row) {                                                      \
-      const Tile tl = row_tile(p, rank);                              \
-      __VA_ARGS__                                                     \
-    } else {                                                          \
-      for (int64_t f_ = f0; f_ < f1;) {                               \
-        const Tile tl = column_tile(p, f_, f1);                       \
-        __VA_ARGS__                                                   \
-      }                                                               \
-    }                                                                 \
-  } while (0)
 
 template <bool F8>
 __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
@@ -823,9 +671,9 @@ tp_status launch_skinny_mode(const LinearProblem& p, cudaStream_t stream) {
     bool ok;
     if (F8) {  // e4m3 codes: one byte per weight
       ok = make_tma_map_u8(&sp.tmW16[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)p.K,
-                           SK_RAW_ROW_BYTES, 16) &&
+                           SK_RAW_ROW_BYTES, 16, false) &&
            make_tma_map_u8(&sp.tmW64[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)p.K,
-                           SK_RAW_ROW_BYTES, 64);
+                           SK_RAW_ROW_BYTES, 64, false);
     } else {
       ok = make_tma_map_bf16(&sp.tmW16[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 16) &&
            make_tma_map_bf16(&sp.tmW64[i], p.W[i], (uint64_t)p.K, rows, (uint64_t)(p.K * es), 64);

@@ -40,7 +40,7 @@ bool make_tma_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint6
 }
 
 bool make_tma_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                     uint64_t ld_bytes, uint32_t box_inner, uint32_t box_rows) {
+                     uint64_t ld_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, rows};
@@ -48,7 +48,8 @@ bool make_tma_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

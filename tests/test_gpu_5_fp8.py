@@ -9,9 +9,10 @@
   weights itself; nothing it uses comes from the GPU.  Tolerance: the bf16
   one (5e-3 x RMS, fp32 output); the FFN's h (bf16) within half a bf16 ulp.
 * The FP8 column split is bit-identical to tp = 1, as the bf16 one is.
-* Both kernels are covered: the FP8 GEMV (one or two tokens) and the tensor-
-  core decode kernel in its FP8 mode (3..128 tokens), which widens the codes
-  to bf16 in shared memory: every one of the 254 finite e4m3 codes goes
+* All three FP8 kernels are covered: the FP8 GEMV (one or two tokens), the
+  tensor-core kernel that widens the codes into tensor memory (3..64 tokens)
+  and the tensor-core decode kernel in its FP8 mode, which widens them into
+  shared memory (65..128 tokens): every one of the 254 finite e4m3 codes goes
   through each kernel once and must come out as its exact value.
 """
 import numpy as np
@@ -149,7 +150,7 @@ def e4m3_table() -> np.ndarray:
     return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 100])
 def test_every_e4m3_code_exact(orc, M):
     """W[n, k] = the value of code (n + k) mod 256 (NaN codes -> +-448), so every
     row holds 448, its scale is 1 and its codes are the table itself; token m is
