@@ -35,19 +35,20 @@
 //                     the cluster adds the partials in rank order through
 //                     distributed shared memory, plus the bias once.
 //
-// Roles (704 threads, one CTA per SM):
+// Roles (736 threads, one CTA per SM):
 //   warp 0      TMA producer: code boxes (128 codes = two k-blocks per row,
 //               128-byte swizzle, one box per lane) into a ring of raw stages,
 //               and one X box {64, np} per k-block into the X ring;
-//   warp 1      TMEM allocation (512 columns: two A buffers of 4 x 32
-//               columns, then D at column 256, np columns per group) and the
-//               MMA thread;
+//   warp 1      TMEM allocation (512 columns: A buffers in columns 0-255 --
+//               two of 4 groups x 32 columns for column tiles, four of 2
+//               groups for row tiles -- then D at column 256, np columns per
+//               group) and the first MMA thread; warp 22 holds the second;
 //   warps 2-5   epilogue (lane quarter = warp mod 4): scale, bias,
 //               activation, stores; row side: partials to shared memory;
 //   warps 6-21  converters: warp w widens group (w - 6) / 4, lane quarter
 //               w mod 4 -- each thread one weight row, 64 codes per k-block:
 //               four swizzled 16-byte shared loads, 32 bf16x2 words, one
-//               tcgen05.st of 32 columns into A buffer n mod 2.
+//               tcgen05.st of 32 columns into A buffer n mod (A buffers).
 // Every wait is bounded (sync.cuh); a wait that gives up records the error
 // and that role stops issuing work, and every thread still reaches the
 // cluster barriers and the TMEM release.
@@ -70,23 +71,30 @@ using namespace decode;
 constexpr int TF_EPI_WARP0 = 2;
 constexpr int TF_CONV_WARP0 = 6;
 constexpr int TF_CONV_WARPS = 16;
-constexpr int TF_THREADS = 32 * (TF_CONV_WARP0 + TF_CONV_WARPS);
+constexpr int TF_ISSUERS = 2;              // MMA threads: warp 1, then warps TF_MMA2_WARP ..
+constexpr int TF_MMA2_WARP = TF_CONV_WARP0 + TF_CONV_WARPS;
+constexpr int TF_THREADS = 32 * (TF_MMA2_WARP + TF_ISSUERS - 1);
 constexpr int TF_GROUPS = 4;               // 128-lane MMA groups per tile (512 rows)
 constexpr int TF_BK = 64;                  // k per k-block (four K=16 MMAs)
 constexpr int TF_KPR = 2;                  // k-blocks per raw stage
 constexpr int TF_RAW_ROW = TF_BK * TF_KPR;  // 128 bytes of codes per raw row
 constexpr int TF_X_ROW = 128;              // bytes per staged X row (64 bf16)
 constexpr int TF_A_COLS = 32;              // TMEM columns of one group's A k-block
-constexpr int TF_ABUFS = 2;
-constexpr int TF_D_BASE = TF_ABUFS * TF_GROUPS * TF_A_COLS;  // 256
+// A buffers: 256 TMEM columns hold 256 / (32 x groups per tile) k-blocks of
+// A -- two for 4-group column tiles, four for the row side's 2-group tiles --
+// so the converters can run that many k-blocks ahead of the MMAs.
+constexpr int TF_A_REGION = 256;
+constexpr int TF_MAX_ABUFS = 4;
+constexpr int TF_D_BASE = TF_A_REGION;
 constexpr int TF_MAX_NP = 64;
 constexpr int TF_TMEM_COLS = 512;
 static_assert(TF_D_BASE + TF_GROUPS * TF_MAX_NP <= TF_TMEM_COLS, "TMEM budget");
+static_assert(TF_A_REGION / (TF_A_COLS * 2) <= TF_MAX_ABUFS, "A buffers of 2-group tiles");
 static_assert(TF_CONV_WARPS == 4 * TF_GROUPS, "one converter warp per (group, lane quarter)");
 constexpr int TF_MAX_STAGES = 16;
 constexpr int TF_MAX_CLUSTER = kSkinnyMaxCluster;
 constexpr int TF_RED_PITCH = SK_BN + 4;    // floats per token row of a reduction buffer
-constexpr int TF_NUM_BARS = 4 * TF_MAX_STAGES + 2 * TF_ABUFS + 3;
+constexpr int TF_NUM_BARS = 4 * TF_MAX_STAGES + 2 * TF_MAX_ABUFS + 3;
 constexpr int TF_BAR_BYTES = TF_NUM_BARS * 8 + 16;
 constexpr int TF_SMEM_MAX = 232448;
 
@@ -109,6 +117,8 @@ struct Fp8TmemParams {
   int tile_cap;                  // column: features (SwiGLU) or rows per tile
   int kb_per_shard, kb_total;
   int cs;                        // row side: CTAs per cluster splitting K
+  int tgroups;                   // MMA groups a tile can use: 4 (column), 2 (row)
+  int abufs;                     // A buffers: TF_A_REGION / (32 x tgroups)
 };
 
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -158,8 +168,8 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
   uint64_t* rfull = bars + 2 * TF_MAX_STAGES;       // codes landed
   uint64_t* rempty = bars + 3 * TF_MAX_STAGES;      // codes read by the converters
   uint64_t* cfull = bars + 4 * TF_MAX_STAGES;       // A buffer written (TMEM)
-  uint64_t* cempty = cfull + TF_ABUFS;              // A buffer consumed by the MMAs
-  uint64_t* tfull = cempty + TF_ABUFS;              // accumulators final
+  uint64_t* cempty = cfull + TF_MAX_ABUFS;          // A buffer consumed by the MMAs
+  uint64_t* tfull = cempty + TF_MAX_ABUFS;          // accumulators final
   uint64_t* tempty = tfull + 1;                     // accumulators read out
   uint64_t* drain = tempty + 1;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + TF_NUM_BARS);
@@ -175,19 +185,19 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), TF_ISSUERS);  // one commit per MMA thread
     }
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&rfull[s]), 1);
       mbar_init(smem_u32(&rempty[s]), TF_CONV_WARPS);
     }
-    for (int b = 0; b < TF_ABUFS; ++b) {
+    for (int b = 0; b < p.abufs; ++b) {
       mbar_init(smem_u32(&cfull[b]), TF_CONV_WARPS);
-      mbar_init(smem_u32(&cempty[b]), 1);
+      mbar_init(smem_u32(&cempty[b]), TF_ISSUERS);
     }
-    mbar_init(smem_u32(tfull), 1);
+    mbar_init(smem_u32(tfull), TF_ISSUERS);
     mbar_init(smem_u32(tempty), 4);  // one arrive per epilogue warp
-    mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(drain), TF_ISSUERS);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -288,8 +298,14 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
         }
       }
     });
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if ((warp == 1 || warp >= TF_MMA2_WARP) && lane == 0) {
+    // ------------------------------------------------------------ MMA issuers
+    // TF_ISSUERS threads take turns over the active groups of every k-block, each waiting
+    // on the same barriers and committing its own MMAs (the barriers count
+    // both).  While one waits on a barrier or commits, the other's MMAs keep
+    // the tensor core busy: the queue in front of it is short, and each
+    // wait costs about as long as an MMA.
+    const int issuer = warp == 1 ? 0 : 1 + warp - TF_MMA2_WARP;
     int xs = 0, buf = 0;
     uint32_t xphase = 0, cphase = 0, tphase = 0;
     bool ok = true;
@@ -310,9 +326,11 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
           }
           tc_fence_after();
           const uint64_t bdesc = sdesc_sw128(smem_u32(sX + (size_t)xs * p.x_stage_bytes));
+          int nth = 0;  // index of the group among the tile's active groups
           for (int g = 0; g < TF_GROUPS; ++g) {
             if (!group_active(g, tl.rows, swiglu)) continue;
-            const uint32_t a0 = tmem_base + (uint32_t)((buf * TF_GROUPS + g) * TF_A_COLS);
+            if ((nth++ % TF_ISSUERS) != issuer) continue;
+            const uint32_t a0 = tmem_base + (uint32_t)((buf * p.tgroups + g) * TF_A_COLS);
             const uint32_t d = tmem_base + (uint32_t)(TF_D_BASE + g * p.np);
 #pragma unroll
             for (int k = 0; k < TF_BK / 16; ++k) {
@@ -327,7 +345,7 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
             xs = 0;
             xphase ^= 1u;
           }
-          if (++buf == TF_ABUFS) {
+          if (++buf == p.abufs) {
             buf = 0;
             cphase ^= 1u;
           }
@@ -420,7 +438,7 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
       }
       tphase ^= 1u;
     });
-  } else if (warp >= TF_CONV_WARP0) {
+  } else if (warp >= TF_CONV_WARP0 && warp < TF_CONV_WARP0 + TF_CONV_WARPS) {
     // ------------------------------------------------------------ converters
     const int cw = warp - TF_CONV_WARP0;
     const int g = cw >> 2;        // MMA group
@@ -468,12 +486,12 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
                 e4m3x4_to_bf16x4(qv.w, w[8 * c + 6], w[8 * c + 7]);
               }
               // word i = bf16 pair (k = 2i, 2i + 1), the lower k in the low half
-              tmem_st32(tcol + (uint32_t)(buf * TF_GROUPS * TF_A_COLS), w);
+              tmem_st32(tcol + (uint32_t)(buf * p.tgroups * TF_A_COLS), w);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&cfull[buf]));
-            if (++buf == TF_ABUFS) {
+            if (++buf == p.abufs) {
               buf = 0;
               cphase ^= 1u;
             }
@@ -598,6 +616,8 @@ tp_status launch_decode_fp8(const LinearProblem& p, cudaStream_t stream) {
     fp.tile_cap = (int)std::min<int64_t>(cap, max_range);
     tile_rows = swiglu ? 2 * fp.tile_cap : fp.tile_cap;
   }
+  fp.tgroups = p.row ? 2 : TF_GROUPS;
+  fp.abufs = TF_A_REGION / (TF_A_COLS * fp.tgroups);
   fp.raw_stage_bytes = tile_rows * TF_RAW_ROW;
   fp.x_stage_bytes = np * TF_X_ROW;
   fp.xstages = std::max(2, std::min(TF_MAX_STAGES, 32768 / fp.x_stage_bytes));
