@@ -55,7 +55,8 @@ COLUMN_CASES = [(1, 256, 96, 2, "none", True), (2, 512, 384, 4, "gelu", True),
                 (5, 1024, 600, 3, "gelu", False), (8, 256, 520, 4, "swiglu", False),
                 (1, 4096, 2048, 8, "swiglu", False), (3, 320, 48, 1, "none", False),
                 (16, 1024, 1000, 4, "gelu", True), (64, 512, 2304, 2, "swiglu", False),
-                (128, 256, 384, 3, "none", True), (33, 2048, 4096, 8, "swiglu", False)]
+                (128, 256, 384, 3, "none", True), (33, 2048, 4096, 8, "swiglu", False),
+                (5, 272, 64, 2, "gelu", True), (70, 336, 512, 2, "swiglu", False)]
 
 
 @pytest.mark.parametrize("M,K,N,tp,act,bias", COLUMN_CASES)
@@ -86,7 +87,8 @@ def test_fp8_column_parallel(orc, M, K, N, tp, act, bias):
 # M, K, N, tp, bias  (tp = 16 row calls with M > 2 take the GEMV)
 ROW_CASES = [(1, 512, 64, 2, True), (3, 1536, 200, 3, False), (8, 4096, 256, 8, True),
              (16, 1024, 520, 4, True), (64, 2048, 1024, 2, False), (128, 512, 300, 1, True),
-             (5, 4096, 96, 16, True), (40, 3072, 768, 6, False)]
+             (5, 4096, 96, 16, True), (40, 3072, 768, 6, False), (4, 544, 320, 2, True),
+             (90, 672, 136, 2, False)]
 
 
 @pytest.mark.parametrize("M,K,N,tp,bias", ROW_CASES)
