@@ -123,12 +123,9 @@ constexpr int SK_THREADS_F8 = SK_THREADS + 32 * SK_CONV_WARPS;
 constexpr int SK_BK = 64;                   // k per stage: one 128-byte swizzle span
 constexpr int SK_UMMA_K = 16;
 constexpr int SK_ROW_BYTES = SK_BK * 2;     // 128 bytes per staged bf16 row
-// FP8 mode: a raw stage holds SK_F8_KPR k-blocks of each tile row, so that
-// every TMA row request moves SK_F8_KPR x 64 contiguous bytes of codes
-#ifndef SK_F8_KPR
-#define SK_F8_KPR 2
-#endif
-constexpr int SK_KPR = SK_F8_KPR;
+// FP8 mode: a raw stage holds SK_KPR k-blocks of each tile row, so that
+// every TMA row request moves SK_KPR x 64 contiguous bytes of codes
+constexpr int SK_KPR = 2;
 static_assert(SK_KPR == 1 || SK_KPR == 2 || SK_KPR == 4, "k-blocks per raw stage");
 constexpr int SK_RAW_ROW_BYTES = SK_BK * SK_KPR;  // bytes per staged row of codes
 constexpr int SK_CSTAGES = 2;               // FP8 mode: bf16 B-tile buffers, one per group
