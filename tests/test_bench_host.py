@@ -34,3 +34,14 @@ def test_work_model_covers_every_workload():
     # the uneven split's widths cover d_ff
     w = bench.WORKLOADS["column_uneven_decode_tp3_b8"]
     assert sum(w["widths"]) == w["dff"] and len(w["widths"]) == w["tp"]
+
+
+def test_fp8_work_model_halves_weight_bytes():
+    """FP8 workloads stream one byte per weight plus one fp32 scale per weight
+    row (per shard on the row side); FLOPs are unchanged."""
+    bf = bench.kernel_work(bench.WORKLOADS["swiglu_ffn_decode_tp4_b1"])
+    f8 = bench.kernel_work(bench.WORKLOADS["swiglu_ffn_decode_tp4_b1_fp8"])
+    d, dff, tp = 8192, 28672, 4
+    assert f8["column"][0] == bf["column"][0] and f8["row"][0] == bf["row"][0]
+    assert f8["column"][1] == bf["column"][1] - 2 * dff * d + 4 * 2 * dff
+    assert f8["row"][1] == bf["row"][1] - dff * d + 4 * tp * d
