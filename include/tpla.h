@@ -69,7 +69,8 @@ typedef enum {
   TP_ERR_ALIGNMENT = 5,       /* pointer or stride not 16-byte aligned */
   TP_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed */
   TP_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device-side wait gave up */
-  TP_ERR_UNSUPPORTED = 8      /* valid but not offered (e.g. a bias where none is defined) */
+  TP_ERR_UNSUPPORTED = 8,     /* valid but not offered (e.g. a bias where none is defined) */
+  TP_ERR_DEVICE_CHECK = 9     /* checked build only: a kernel's index check failed (access skipped) */
 } tp_status;
 
 typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
@@ -515,7 +516,10 @@ tp_status tp_mlp_block_noalloc(int tp, int64_t M, int64_t d_model, int64_t d_ff,
  * inside the library's kernels is bounded; a wait that runs out sets this
  * word and the kernel returns early (its output is then incomplete).
  * Returns TP_OK, TP_ERR_DEVICE_TIMEOUT, or TP_ERR_CUDA if the stream itself
- * reports an error.
+ * reports an error.  A checked build of the library (libtpla_checked.so,
+ * compiled with TPLA_CHECKED) also checks the kernels' computed shared-memory,
+ * tensor-memory and weight-row indices; a failed check skips the access and
+ * is reported here as TP_ERR_DEVICE_CHECK.
  */
 tp_status tp_device_status(tp_stream_t stream);
 

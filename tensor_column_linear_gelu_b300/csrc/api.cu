@@ -236,6 +236,8 @@ const char* tp_status_string(tp_status s) {
     case TP_ERR_CUDA: return "TP_ERR_CUDA: a CUDA call failed";
     case TP_ERR_DEVICE_TIMEOUT: return "TP_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
     case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED: argument combination not offered";
+    case TP_ERR_DEVICE_CHECK:
+      return "TP_ERR_DEVICE_CHECK: a kernel index check failed (checked build; access skipped)";
   }
   return "unknown tp_status";
 }

@@ -119,6 +119,7 @@ struct Fp8TmemParams {
   int cs;                        // row side: CTAs per cluster splitting K
   int tgroups;                   // MMA groups a tile can use: 4 (column), 2 (row)
   int abufs;                     // A buffers: TF_A_REGION / (32 x tgroups)
+  int ring_bytes;                // shared memory below the barriers (checked builds)
 };
 
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -230,16 +231,18 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
     SK_FOR_EACH_TILE(tl, {
       if (ok) {
         int piece = 0, half = 0, r = 0, h = 0;
-        const bool mine = lane > 0 && tile_box(tl, swiglu, lane - 1, piece, half, r, h);
+        const bool has_box = lane > 0 && tile_box(tl, swiglu, lane - 1, piece, half, r, h);
         int64_t wrow = 0;   // first weight row of this lane's box in its shard buffer
         uint32_t woff = 0;  // its offset in the raw stage
         int wshard = 0;
-        if (mine) {
+        if (has_box) {
           const Piece& pc = tl.pc[piece];
           wrow = (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G + half * G : pc.loc) + r;
           woff = (uint32_t)(pc.slot + half * tl.rows + r) * TF_RAW_ROW;
           wshard = pc.shard;
         }
+        const bool mine =
+            has_box && TP_CHECK(p.err, woff + (uint32_t)h * TF_RAW_ROW <= (uint32_t)p.raw_stage_bytes);
         uint32_t wbytes = 0;
         if (lane == 0) {
           for (int b = 0; b < tl.boxes; ++b) {
@@ -330,6 +333,9 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
           for (int g = 0; g < TF_GROUPS; ++g) {
             if (!group_active(g, tl.rows, swiglu)) continue;
             if ((nth++ % TF_ISSUERS) != issuer) continue;
+            if (!TP_CHECK(p.err, (buf * p.tgroups + g + 1) * TF_A_COLS <= TF_A_REGION &&
+                                     TF_D_BASE + (g + 1) * p.np <= TF_TMEM_COLS))
+              continue;
             const uint32_t a0 = tmem_base + (uint32_t)((buf * p.tgroups + g) * TF_A_COLS);
             const uint32_t d = tmem_base + (uint32_t)(TF_D_BASE + g * p.np);
 #pragma unroll
@@ -422,7 +428,8 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
                 const int64_t t = t0 + j;
                 if (t >= p.M) break;
                 if (p.row && p.cs > 1) {
-                  red[t * TF_RED_PITCH + s] = v[j];  // this rank's partial, slot = output
+                  if (TP_CHECK(p.err, (t * TF_RED_PITCH + s + 1) * 4 <= p.ring_bytes))
+                    red[t * TF_RED_PITCH + s] = v[j];  // this rank's partial, slot = output
                 } else if (p.row) {
                   store_out(p.Y, p.ydt, t * p.ldy + n, v[j]);
                 } else {
@@ -450,8 +457,10 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
       if (ok) {
         const bool active = group_active(g, tl.rows, swiglu);          // warp-uniform
         const int s = (swiglu ? (g & 1) : g) * 128 + q * 32 + lane;    // slot
-        const bool valid = active && s < tl.rows;
         const int rraw = (swiglu && g >= 2) ? tl.rows + s : s;         // raw stage row
+        const bool valid =
+            active && s < tl.rows &&
+            TP_CHECK(p.err, (int64_t)(rraw + 1) * TF_RAW_ROW <= p.raw_stage_bytes);
         const uint32_t tcol = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * TF_A_COLS);
         for (int kb = tl.kb0; kb < tl.kb1 && ok; kb += TF_KPR) {
           const int nsub = tl.kb1 - kb < TF_KPR ? tl.kb1 - kb : TF_KPR;
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
               ok = false;
               break;
             }
-            if (active) {
+            if (active && TP_CHECK(p.err, (buf * p.tgroups + g + 1) * TF_A_COLS <= TF_A_REGION)) {
               // k-block j of the row: 16-byte chunks 4j .. 4j+3, each stored at
               // chunk (c ^ (row mod 8)) by the 128-byte swizzle
               uint32_t w[32];
@@ -627,6 +636,7 @@ tp_status launch_decode_fp8(const LinearProblem& p, cudaStream_t stream) {
   if (stages < 2) return TP_ERR_UNSUPPORTED;
   fp.stages = stages;
   const int ring = xring + stages * fp.raw_stage_bytes;
+  fp.ring_bytes = ring;
   if (p.row && fp.cs > 1 && (int64_t)p.M * TF_RED_PITCH * 4 > ring) return TP_ERR_UNSUPPORTED;
   const int smem = 1024 + ring + TF_BAR_BYTES;
 

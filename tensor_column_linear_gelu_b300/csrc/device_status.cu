@@ -52,6 +52,7 @@ tp_status read_and_clear_device_error(cudaStream_t stream) {
     return TP_ERR_CUDA;
   if (cudaMemsetAsync(w, 0, sizeof(v), stream) != cudaSuccess) return TP_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return TP_ERR_CUDA;
+  if (v & kErrIndexCheck) return TP_ERR_DEVICE_CHECK;
   return v ? TP_ERR_DEVICE_TIMEOUT : TP_OK;
 }
 

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sync.cuh"
 
 namespace tpla {
 namespace {
@@ -77,6 +78,8 @@ struct Fp8Params {
   const float* S[TP_MAX_TP];   // row scales of each shard buffer
   const float* bias[TP_MAX_TP];
   void* Y;
+  int64_t wrows[TP_MAX_TP];    // rows of each code buffer (checked builds)
+  unsigned int* err;           // device error word (checked builds)
 };
 
 __device__ __forceinline__ void fp8x16_to_float(const uint4& v, float (&f)[16]) {
@@ -166,6 +169,7 @@ __global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constan
           const int64_t n = o - p.fo[i];
           int64_t row = n;
           if constexpr (SW) row = (n / G) * 2 * G + n % G;
+          if (!TP_CHECK(p.err, row + (SW ? G : 0) < p.wrows[i])) row = 0;
           wr[r] = p.W[i] + row * p.K;
           sc[r] = __ldg(p.S[i] + row);
           if constexpr (SW) {
@@ -183,7 +187,8 @@ __global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constan
           float part[MT][NR];
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            const int64_t o = min(t * R + r, p.n_out - 1);
+            int64_t o = min(t * R + r, p.n_out - 1);
+            if (!TP_CHECK(p.err, o < p.wrows[i])) o = 0;
             wr[r] = p.W[i] + o * p.K;
             sc[r] = __ldg(p.S[i] + o);
           }
@@ -295,6 +300,8 @@ tp_status launch_gemv_fp8(const LinearProblem& p, cudaStream_t stream) {
   for (int i = 0; i < p.tp; ++i) gp.yoff[i] = p.yoff[i];
   gp.X = static_cast<const __nv_bfloat16*>(p.X);
   gp.Y = p.Y;
+  for (int i = 0; i < p.tp; ++i) gp.wrows[i] = p.row ? p.w_rows : p.wr[i];
+  gp.err = device_error_word();
   for (int i = 0; i < TP_MAX_TP; ++i) {
     gp.W[i] = static_cast<const uint8_t*>(p.W[i]);
     gp.S[i] = p.wscale[i];

@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sync.cuh"
 
 namespace tpla {
 namespace {
@@ -44,6 +45,8 @@ struct GemvParams {
   const void* W[TP_MAX_TP];
   const float* bias[TP_MAX_TP];
   void* Y;
+  int64_t wrows[TP_MAX_TP];   // rows of each weight shard buffer (checked builds)
+  unsigned int* err;          // device error word (checked builds)
 };
 
 template <typename T>
@@ -145,11 +148,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
           const T* Wi = reinterpret_cast<const T*>(p.W[i]);
           if constexpr (SW) {
             const int64_t grp = n / G;
-            const int64_t row = grp * 2 * G + (n - grp * G);
+            int64_t row = grp * 2 * G + (n - grp * G);
+            if (!TP_CHECK(p.err, row + G < p.wrows[i])) row = 0;
             wr[r] = Wi + row * p.K;
             wr[R + r] = Wi + (row + G) * p.K;
           } else {
-            wr[r] = Wi + n * p.K;
+            wr[r] = Wi + (TP_CHECK(p.err, n < p.wrows[i]) ? n : 0) * p.K;
           }
         }
         for (int64_t c0 = lane; c0 < nvec; c0 += 32 * U)
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
 #pragma unroll
           for (int r = 0; r < R; ++r) {
             const int64_t o = min(t * R + r, p.n_out - 1);
-            wr[r] = Wi + o * p.K;
+            wr[r] = Wi + (TP_CHECK(p.err, o < p.wrows[i]) ? o : 0) * p.K;
           }
           const T* xi = X + i * p.x_shard_off;
           for (int64_t c0 = lane; c0 < nvec; c0 += 32 * U)
@@ -265,6 +269,8 @@ tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream) {
     gp.W[i] = p.W[i];
     gp.bias[i] = p.bias[i];
   }
+  for (int i = 0; i < p.tp; ++i) gp.wrows[i] = p.row ? p.w_rows : p.wr[i];
+  gp.err = device_error_word();
   if (p.xdt == TP_F32) return dispatch_act<float>(p, gp, stream);
   return dispatch_act<__nv_bfloat16>(p, gp, stream);
 }

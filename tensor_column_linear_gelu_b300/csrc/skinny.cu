@@ -163,6 +163,7 @@ struct SkinnyParams {
   int acc_stride, acc_bufs;      // TMEM columns per accumulator buffer, buffers
   int kb_per_shard, kb_total;
   int cs;                        // row side: CTAs per cluster splitting K
+  int ring_bytes;                // shared memory below the barriers (checked builds)
 };
 
 template <bool F8>
@@ -260,17 +261,20 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
     SK_FOR_EACH_TILE(tl, {
       if (ok) {
         int piece = 0, half = 0, r = 0, h = 0;
-        const bool mine = lane > 0 && tile_box(tl, swiglu, lane - 1, piece, half, r, h);
+        const bool has_box = lane > 0 && tile_box(tl, swiglu, lane - 1, piece, half, r, h);
         int64_t wrow = 0;     // first weight row of this lane's box in its shard buffer
         uint32_t woff = 0;    // its offset in the stage's B tile
         int wshard = 0;
         constexpr int pitch = F8 ? SK_RAW_ROW_BYTES : SK_ROW_BYTES;  // bytes per loaded row
-        if (mine) {
+        if (has_box) {
           const Piece& pc = tl.pc[piece];
           wrow = (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G + half * G : pc.loc) + r;
           woff = (uint32_t)(pc.slot + half * tl.rows + r) * pitch;
           wshard = pc.shard;
         }
+        const bool mine =
+            has_box && TP_CHECK(p.err, woff + (uint32_t)h * pitch <=
+                                           (uint32_t)(F8 ? p.raw_stage_bytes : p.w_stage_bytes));
         uint32_t wbytes = 0;  // weight (code) bytes of one stage
         if (lane == 0) {
           for (int b = 0; b < tl.boxes; ++b) {
@@ -386,7 +390,10 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
         const uint32_t idesc0 = idesc_bf16_f32(128, n0);
         const uint32_t idesc1 = idesc_bf16_f32(128, n1 > 0 ? n1 : 16);
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.acc_stride);
-        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+        if (!TP_CHECK(p.err, nrows * SK_ROW_BYTES <= p.w_stage_bytes &&
+                                 acc * p.acc_stride + nrows <= SK_TMEM_COLS))
+          ok = false;
+        for (int kb = tl.kb0; ok && kb < tl.kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase) ||
               (F8 && !mbar_wait_bounded(smem_u32(&cfull[cst]), cphase))) {
             report_error(p.err, kErrTimeoutMma);
@@ -465,7 +472,8 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
               for (int j = 0; j < 8; ++j)
                 if (j0 + j < c) v[j] *= __ldg(sc + j);
             }
-            if (t < p.M) {
+            if (t < p.M &&
+                TP_CHECK(p.err, (int64_t)(t * SK_RED_PITCH + j0 + 8) * 4 <= p.ring_bytes)) {
               float4* dst = reinterpret_cast<float4*>(red + t * SK_RED_PITCH + j0);
               dst[0] = make_float4(v[0], v[1], v[2], v[3]);
               dst[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -554,6 +562,9 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
     SK_FOR_EACH_TILE(tl, {
       if (ok) {
         const int nrows = swiglu ? 2 * tl.rows : tl.rows;
+        if (!TP_CHECK(p.err, nrows * SK_RAW_ROW_BYTES <= p.raw_stage_bytes &&
+                                 nrows * SK_ROW_BYTES <= p.w_stage_bytes))
+          ok = false;
         for (int kb = tl.kb0; kb < tl.kb1 && ok; kb += SK_KPR) {
           const int nsub = tl.kb1 - kb < SK_KPR ? tl.kb1 - kb : SK_KPR;
           bool got = mbar_wait_bounded(smem_u32(&rfull[rs]), rphase);
@@ -747,6 +758,7 @@ tp_status launch_skinny_mode(const LinearProblem& p, cudaStream_t stream) {
   if (stages < 2) return TP_ERR_UNSUPPORTED;
   sp.stages = stages;
   const int ring = stages * per_stage + fixed;
+  sp.ring_bytes = ring;
   const int x_ring_stages = F8 ? sp.xstages : stages;
   // The MMA reads a full 128-row A tile from each X stage: the read past the
   // last X stage runs into the stages after the X ring (weights, or codes in

@@ -22,6 +22,7 @@ enum : uint32_t {
   kErrTimeoutDrain = 1u << 3,
   kErrSelftest = 1u << 4,
   kErrTimeoutConvert = 1u << 5,
+  kErrIndexCheck = 1u << 6,  // checked builds: an index check failed
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -90,5 +91,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void report_error(unsigned int* err, uint32_t code) {
   if (err) atomicOr(err, code);
 }
+
+// Index checks of checked builds (-DTPLA_CHECKED): TP_CHECK(err, cond) is true
+// when cond holds; otherwise it records kErrIndexCheck in the device error
+// word and is false, and the caller skips the access.  In release builds it
+// is the constant true and compiles away.  (No assert or trap: a failed check
+// leaves the context usable and surfaces as TP_ERR_DEVICE_CHECK.)
+#ifdef TPLA_CHECKED
+#define TP_CHECK(err, cond) ((cond) || (::tpla::report_error((err), ::tpla::kErrIndexCheck), false))
+#else
+#define TP_CHECK(err, cond) true
+#endif
 
 }  // namespace tpla

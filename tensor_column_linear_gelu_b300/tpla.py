@@ -15,12 +15,15 @@ from typing import Optional, Sequence
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtpla.so")
+# TPLA_CHECKED=1 loads the checked build of the same library (index checks in
+# the kernels, reported as TP_ERR_DEVICE_CHECK); it must have been built.
+CHECKED = os.environ.get("TPLA_CHECKED") == "1"
+LIB_PATH = os.path.join(_PKG, "libtpla_checked.so" if CHECKED else "libtpla.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m tensor_column_linear_gelu_b300.build` "
-        "(nvcc, sm_103a). There is no fallback path.")
+        f"{LIB_PATH} is missing: build it with `python -m tensor_column_linear_gelu_b300.build"
+        f"{' --checked' if CHECKED else ''}` (nvcc, sm_103a). There is no fallback path.")
 
 lib = ctypes.CDLL(LIB_PATH)
 
@@ -28,6 +31,7 @@ lib = ctypes.CDLL(LIB_PATH)
 TP_OK = 0
 TP_ERR_NULL, TP_ERR_NOT_DIVISIBLE, TP_ERR_BAD_SHAPE, TP_ERR_DTYPE = 1, 2, 3, 4
 TP_ERR_ALIGNMENT, TP_ERR_CUDA, TP_ERR_DEVICE_TIMEOUT, TP_ERR_UNSUPPORTED = 5, 6, 7, 8
+TP_ERR_DEVICE_CHECK = 9
 TP_F32, TP_BF16 = 0, 1
 TP_ACT_NONE, TP_ACT_GELU_ERF, TP_ACT_SWIGLU = 0, 1, 2
 TP_SPLIT_COLUMN, TP_SPLIT_ROW, TP_SPLIT_QKV_HEADS, TP_SPLIT_GATE_UP = 0, 1, 2, 3

@@ -40,6 +40,27 @@ def test_library_exports_every_declared_symbol():
     assert set(tpla.EXPORTS) == set(declared_functions())
 
 
+def test_checked_build_exports_the_same_symbols():
+    """libtpla_checked.so (the kernels with index checks, loaded when
+    TPLA_CHECKED=1) is built beside the release library and exports the same
+    entry points."""
+    from tensor_column_linear_gelu_b300 import build
+    path = build.build(checked=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, name
+    code = ("import os; os.environ['TPLA_CHECKED'] = '1'\n"
+            "from tensor_column_linear_gelu_b300 import tpla\n"
+            "assert tpla.CHECKED and tpla.LIB_PATH.endswith('libtpla_checked.so')\n"
+            "print(tpla.status_string(tpla.TP_ERR_DEVICE_CHECK))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.startswith("TP_ERR_DEVICE_CHECK")
+
+
 def test_shard_shape():
     from tensor_column_linear_gelu_b300 import tpla
     assert tpla.tp_shard_shape("column", 2, 6, 8) == (3, 8)
