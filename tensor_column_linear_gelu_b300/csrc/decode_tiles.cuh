@@ -4,7 +4,8 @@
 // the e4m3 -> bf16 widening, and the tiling of a CTA's outputs into pieces
 // of consecutive features at 16-row slots.  The tiling functions take any
 // parameter struct with the fields they read (tile_cap, act, tp, fo,
-// kb_total, feat_total, cs).
+// kb_total, feat_total, cs).  The tiling is host-callable as well
+// (TILE_FN), so a host program can check it over whole grids.
 #pragma once
 
 #include <cstdint>
@@ -20,7 +21,9 @@ constexpr int SK_BN = 256;                  // outputs per row-side tile
 constexpr int64_t G = TP_GATE_UP_GROUP;
 static_assert(2 * G == SK_BN, "a gate/up group's rows fill one 256-row tile");
 
-__device__ __forceinline__ int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
+#define TILE_FN __host__ __device__ __forceinline__
+
+TILE_FN int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
 
 // Byte permute (PTX prmt, default mode): result byte i is byte (sel_i & 7)
 // of {a, 0}, or that byte's sign bit replicated when sel_i & 8.
@@ -73,12 +76,12 @@ struct Tile {
 };
 
 // Weight boxes of a piece of c rows: whole 64-row boxes, then 16-row boxes.
-__device__ __forceinline__ int piece_boxes(int c) { return c / 64 + ((c % 64) + 15) / 16; }
+TILE_FN int piece_boxes(int c) { return c / 64 + ((c % 64) + 15) / 16; }
 
 // Box `want` (0-based) of a tile, in the order pieces, then gate/up halves,
 // then rows: which piece and half, its first row within the piece, and its
 // height.  Returns false when the tile has fewer boxes.
-__device__ __forceinline__ bool tile_box(const Tile& t, bool swiglu, int want, int& piece,
+TILE_FN bool tile_box(const Tile& t, bool swiglu, int want, int& piece,
                                          int& half, int& r, int& h) {
   int b = 0;
   for (int i = 0; i < t.n; ++i)
@@ -102,7 +105,7 @@ __device__ __forceinline__ bool tile_box(const Tile& t, bool swiglu, int want, i
 // Column side: the tile starting at global feature f of a range ending at f1;
 // advances f past the features it takes.
 template <class P>
-__device__ __forceinline__ Tile column_tile(const P& p, int64_t& f, int64_t f1) {
+TILE_FN Tile column_tile(const P& p, int64_t& f, int64_t f1) {
   const bool swiglu = p.act == TP_ACT_SWIGLU;
   const int cap = p.tile_cap;  // slot rows per tile (features for SwiGLU)
   Tile t;
@@ -132,22 +135,27 @@ __device__ __forceinline__ Tile column_tile(const P& p, int64_t& f, int64_t f1) 
   return t;
 }
 
-// Column side: this CTA's feature range [f0, f1), balanced in units of 8.
+// Column side: CTA b of grid's feature range [f0, f1), balanced in units of
+// SK_GRAIN features.
 template <class P>
-__device__ __forceinline__ void column_range(const P& p, int64_t& f0, int64_t& f1) {
+TILE_FN void column_range_of(const P& p, int64_t b, int64_t grid, int64_t& f0, int64_t& f1) {
   const int64_t units = (p.feat_total + SK_GRAIN - 1) / SK_GRAIN;
-  const int64_t u0 = (int64_t)blockIdx.x * units / gridDim.x;
-  const int64_t u1 = ((int64_t)blockIdx.x + 1) * units / gridDim.x;
+  const int64_t u0 = b * units / grid;
+  const int64_t u1 = (b + 1) * units / grid;
   f0 = imin(u0 * SK_GRAIN, p.feat_total);
   f1 = imin(u1 * SK_GRAIN, p.feat_total);
+}
+template <class P>
+__device__ __forceinline__ void column_range(const P& p, int64_t& f0, int64_t& f1) {
+  column_range_of(p, (int64_t)blockIdx.x, (int64_t)gridDim.x, f0, f1);
 }
 
 // Row side: the one tile of this CTA -- its cluster's 256 outputs and its
 // rank's share of the k-blocks.
 template <class P>
-__device__ __forceinline__ Tile row_tile(const P& p, int rank) {
+TILE_FN Tile row_tile_of(const P& p, int64_t block, int rank) {
   Tile t;
-  const int64_t tile = blockIdx.x / p.cs;
+  const int64_t tile = block / p.cs;
   t.n = 1;
   t.pc[0].shard = 0;
   t.pc[0].loc = tile * SK_BN;
@@ -158,6 +166,10 @@ __device__ __forceinline__ Tile row_tile(const P& p, int rank) {
   t.kb0 = (int)((int64_t)rank * p.kb_total / p.cs);
   t.kb1 = (int)((int64_t)(rank + 1) * p.kb_total / p.cs);
   return t;
+}
+template <class P>
+__device__ __forceinline__ Tile row_tile(const P& p, int rank) {
+  return row_tile_of(p, (int64_t)blockIdx.x, rank);
 }
 
 // Loop over this CTA's tiles: the column side walks its feature range, the

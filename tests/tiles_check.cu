@@ -1,0 +1,189 @@
+// tiles_check.cu -- host program (no kernel launch) that runs the decode
+// kernels' tiling (csrc/decode_tiles.cuh) over whole grids, the way the
+// launchers configure it, and checks the index arithmetic the kernels rely on:
+//   column side, every CTA of the grid:
+//     * the CTAs' feature ranges partition [0, F) in SK_GRAIN units;
+//     * a CTA's tiles cover its range in order; each piece lies inside one
+//       shard and, for SwiGLU, inside one gate/up group;
+//     * slots are 16-row aligned and packed; a tile's slot rows never exceed
+//       the tile cap the launcher sized its stages for;
+//     * the boxes tile_box enumerates are at most SK_MAX_BOXES, cover each
+//       piece (and half) exactly in 64- and 16-row boxes, and land inside the
+//       stage's rows; their first weight row lies inside the shard buffer;
+//   row side, every (tile, rank) of the clusters:
+//     * tiles cover [0, N) once; ranks partition the k-blocks; with tp x j
+//       CTAs per cluster (the FP8 kernels) each rank's k-range lies in one
+//       shard.
+// Prints "ok" and exits 0, or prints the first violation and exits 1.
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+
+#include "decode_tiles.cuh"
+
+using namespace tpla::decode;
+
+struct Params {
+  int tile_cap = 0, act = TP_ACT_NONE, tp = 1, cs = 1, kb_total = 1;
+  int64_t feat_total = 0;
+  int64_t fo[TP_MAX_TP + 1] = {};
+};
+
+static int fails = 0;
+#define CHECK(cond, ...)                              \
+  do {                                                \
+    if (!(cond)) {                                    \
+      if (fails++ == 0) {                             \
+        std::printf("FAIL %s:%d: ", __FILE__, __LINE__); \
+        std::printf(__VA_ARGS__);                     \
+        std::printf("\n");                            \
+      }                                               \
+      return;                                         \
+    }                                                 \
+  } while (0)
+
+static int64_t gate_up_rows(int64_t ns) { return 2 * G * ((ns + G - 1) / G); }
+
+// widths: per-shard features; swiglu; cap_features: the launcher's cap.
+static void check_column(const std::vector<int64_t>& widths, bool swiglu, int64_t cap_limit,
+                         int sms) {
+  Params p;
+  p.tp = (int)widths.size();
+  p.act = swiglu ? TP_ACT_SWIGLU : TP_ACT_GELU_ERF;
+  p.fo[0] = 0;
+  for (int i = 0; i < p.tp; ++i) p.fo[i + 1] = p.fo[i] + widths[i];
+  p.feat_total = p.fo[p.tp];
+  const int64_t units = (p.feat_total + SK_GRAIN - 1) / SK_GRAIN;
+  const int64_t grid = units < sms ? units : sms;
+  const int64_t max_range = (units + grid - 1) / grid * SK_GRAIN;
+  p.tile_cap = (int)(cap_limit < max_range ? cap_limit : max_range);
+  const int tile_rows = swiglu ? 2 * p.tile_cap : p.tile_cap;  // stage rows
+  int64_t expect = 0;
+  for (int64_t b = 0; b < grid; ++b) {
+    int64_t f0, f1;
+    column_range_of(p, b, grid, f0, f1);
+    CHECK(f0 == expect, "CTA %lld starts at %lld, expected %lld", (long long)b, (long long)f0,
+          (long long)expect);
+    CHECK(f0 % SK_GRAIN == 0 && f1 >= f0, "CTA %lld range [%lld, %lld)", (long long)b,
+          (long long)f0, (long long)f1);
+    expect = f1;
+    for (int64_t f = f0; f < f1;) {
+      const int64_t start = f;
+      const Tile t = column_tile(p, f, f1);
+      CHECK(t.n >= 1 && f > start, "no progress at feature %lld", (long long)start);
+      CHECK(t.rows <= p.tile_cap, "tile rows %d > cap %d", t.rows, p.tile_cap);
+      CHECK(t.boxes <= SK_MAX_BOXES, "%d boxes", t.boxes);
+      int64_t g = start;
+      int slot = 0, boxes = 0;
+      for (int i = 0; i < t.n; ++i) {
+        const Piece& pc = t.pc[i];
+        CHECK(pc.slot == slot && pc.slot % 16 == 0, "piece %d slot %d, expected %d", i, pc.slot,
+              slot);
+        CHECK(pc.c >= 1, "empty piece");
+        CHECK(p.fo[pc.shard] <= g && g < p.fo[pc.shard + 1], "piece %d in the wrong shard", i);
+        CHECK(pc.loc == g - p.fo[pc.shard], "piece %d loc", i);
+        CHECK(pc.loc + pc.c <= widths[pc.shard], "piece %d crosses its shard's end", i);
+        if (swiglu) CHECK(pc.loc / G == (pc.loc + pc.c - 1) / G, "piece %d crosses a group", i);
+        const int64_t buf_rows = swiglu ? gate_up_rows(widths[pc.shard]) : widths[pc.shard];
+        // this piece's boxes, in tile_box order
+        for (int half = 0; half < (swiglu ? 2 : 1); ++half) {
+          int covered = 0;
+          while (covered < pc.c) {
+            int pi, hf, r, h;
+            CHECK(tile_box(t, swiglu, boxes, pi, hf, r, h), "box %d missing", boxes);
+            CHECK(pi == i && hf == half && r == covered, "box %d is (%d,%d,%d)", boxes, pi, hf, r);
+            CHECK(h == 64 || h == 16, "box height %d", h);
+            CHECK(pc.slot + half * t.rows + r + h <= tile_rows, "box %d leaves the stage", boxes);
+            const int64_t wrow =
+                (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G + half * G : pc.loc) + r;
+            CHECK(wrow < buf_rows, "box %d starts at weight row %lld of %lld", boxes,
+                  (long long)wrow, (long long)buf_rows);
+            covered += h;
+            ++boxes;
+          }
+          CHECK(covered == (pc.c + 15) / 16 * 16 || (covered >= pc.c && covered - pc.c < 16),
+                "piece %d half %d covered %d rows for %d", i, half, covered, pc.c);
+        }
+        g += pc.c;
+        slot += (pc.c + 15) / 16 * 16;
+      }
+      int pi, hf, r, h;
+      CHECK(!tile_box(t, swiglu, boxes, pi, hf, r, h) && boxes == t.boxes, "box count %d vs %d",
+            boxes, t.boxes);
+      CHECK(g == f && slot == t.rows, "tile covers [%lld, %lld), advanced to %lld",
+            (long long)start, (long long)g, (long long)f);
+    }
+  }
+  CHECK(expect == p.feat_total, "ranges end at %lld of %lld", (long long)expect,
+        (long long)p.feat_total);
+}
+
+// n_out outputs, tp shards of kbs k-blocks each, clusters of cs CTAs.
+static void check_row(int64_t n_out, int tp, int kbs, int cs, bool one_shard_per_rank) {
+  Params p;
+  p.tp = tp;
+  p.cs = cs;
+  p.feat_total = n_out;
+  p.kb_total = kbs * tp;
+  const int64_t tiles = (n_out + SK_BN - 1) / SK_BN;
+  int64_t covered = 0;
+  for (int64_t tile = 0; tile < tiles; ++tile) {
+    int next_kb = 0;
+    for (int rank = 0; rank < cs; ++rank) {
+      const Tile t = row_tile_of(p, tile * cs + rank, rank);
+      CHECK(t.n == 1 && t.pc[0].loc == tile * SK_BN, "tile %lld loc", (long long)tile);
+      CHECK(t.pc[0].c >= 1 && t.pc[0].c <= SK_BN && t.rows <= SK_BN, "tile %lld width",
+            (long long)tile);
+      CHECK(t.boxes <= SK_MAX_BOXES, "row tile boxes %d", t.boxes);
+      CHECK(t.kb0 == next_kb && t.kb1 > t.kb0, "rank %d k-range [%d, %d)", rank, t.kb0, t.kb1);
+      next_kb = t.kb1;
+      if (one_shard_per_rank)
+        CHECK(t.kb0 / kbs == (t.kb1 - 1) / kbs, "rank %d k-range [%d, %d) crosses a shard", rank,
+              t.kb0, t.kb1);
+      if (rank == 0) covered += t.pc[0].c;
+    }
+    CHECK(next_kb == p.kb_total, "ranks end at k-block %d of %d", next_kb, p.kb_total);
+  }
+  CHECK(covered == n_out, "tiles cover %lld of %lld outputs", (long long)covered,
+        (long long)n_out);
+}
+
+int main() {
+  const int sms = 148;
+  // decode FFN up projection, d_ff 28672, tp 4 (7168 per shard): bf16 kernel
+  // (cap 256), FP8 shared-memory mode (SwiGLU cap 128), FP8 TMEM kernel
+  // (SwiGLU 256 features, plain 512 rows)
+  check_column({7168, 7168, 7168, 7168}, true, 256, sms);
+  check_column({7168, 7168, 7168, 7168}, true, 128, sms);
+  check_column({7168, 7168, 7168, 7168}, false, 512, sms);
+  // QKV of the 70B attention, tp 8: (64 + 16) heads x 128 / 8 = 1280 per shard
+  check_column(std::vector<int64_t>(8, 1280), false, 256, sms);
+  // the uneven tp=3 split of d_ff 28672, and small ragged test shapes
+  check_column({9558, 9557, 9557}, false, 256, sms);
+  check_column({5, 4}, false, 256, sms);
+  check_column({300, 200, 500}, false, 256, sms);
+  check_column({136, 8, 256, 40}, false, 512, sms);
+  check_column({200, 200, 200}, false, 256, sms);
+  check_column({576, 576}, true, 256, sms);
+  check_column({1152, 1152}, true, 256, sms);
+  check_column({250, 250, 250, 250}, true, 128, sms);
+  check_column({1}, false, 256, sms);
+  check_column({16}, true, 256, sms);
+  for (int tp = 1; tp <= 8; ++tp) check_column(std::vector<int64_t>(tp, 130 * tp + 7), true, 256, sms);
+  // row side: bf16 kernel cs = min(8, 148 / tiles) (capped by the k-blocks);
+  // FP8 kernels cs = tp x j
+  check_row(8192, 4, 112, 4, true);
+  check_row(8192, 8, 56, 4, false);
+  check_row(300, 1, 8, 8, true);
+  check_row(1024, 2, 16, 8, true);
+  check_row(520, 4, 4, 8, true);
+  check_row(768, 6, 8, 6, true);
+  check_row(40, 3, 1, 3, true);
+  check_row(200, 3, 8, 8, false);
+  if (fails) {
+    std::printf("%d violation(s)\n", fails);
+    return 1;
+  }
+  std::printf("ok\n");
+  return 0;
+}
