@@ -289,6 +289,28 @@ def check_ring_allreduce(orc):
         W = _int_mat(rng, (5, 4 * tp), -2, 2)
         b = _int_mat(rng, (5,), -3, 3)
         assert np.array_equal(orc.row_parallel_ring(tp, X, W, b, "bf16"), _brute_linear(X, W, b))
+    # Case D, fp32 wire, worked by hand: tp=3, M=1, K=3, N=3, x = [1,1,1], W
+    # rows [2^24, 1, 1]: P0 = 2^24, P1 = P2 = 1; L = 3, chunk c = element c.
+    # fp32 holds integers exactly up to 2^24 and is spaced by 2 in
+    # [2^24, 2^25); 2^24 + 1 is a tie that rounds to the even significand,
+    # 2^24:
+    #   chunk 0 starts at rank 0: 2^24 + 1 -> 2^24, + 1 -> 2^24;
+    #   chunk 1 starts at rank 1: 1 + 1 = 2, + 2^24 = 2^24 + 2 (exact);
+    #   chunk 2 starts at rank 2: 1 + 2^24 -> 2^24, + 1 -> 2^24.
+    # Without the rounding after each hop every element would be 2^24 + 2.
+    t24 = 2.0 ** 24
+    X = np.ones((1, 3), np.float32)
+    W = np.tile(np.array([[t24, 1, 1]], np.float32), (3, 1))
+    y = orc.row_parallel_ring(3, X, W, None, "f32")
+    assert np.array_equal(y, [[t24, t24 + 2, t24]]), y
+    # Case E, fp32 wire, a partial fp32 cannot hold: tp=2, x = [1,1,1,1], W
+    # row [2^24, 1, 1, 1].  P0 = 2^24 + 1 is held as 2^24 (the tie, to even),
+    # P1 = 2.  Both chunks: 2^24 + 2 (exact).  Unrounded partials would give
+    # 2^24 + 3, a tie that rounds to 2^24 + 4.
+    X = np.ones((1, 4), np.float32)
+    W = np.tile(np.array([[t24, 1, 1, 1]], np.float32), (2, 1))
+    y = orc.row_parallel_ring(2, X, W, None, "f32")
+    assert np.array_equal(y, [[t24 + 2, t24 + 2]]), y
     # fp32 wire: within a few fp32 roundings of the exact sum
     X = rng.standard_normal((4, 96)).astype(np.float32)
     W = rng.standard_normal((7, 96)).astype(np.float32)
@@ -331,6 +353,27 @@ def check_fp8_weights(orc):
     assert all(orc.round_e4m3(float(q)) == q for q in Q.ravel()[:200])
     Q2, S2 = orc.quantize_rows_fp8(2 * W)                # a power of 2 scales exactly
     assert np.array_equal(Q2, Q) and np.array_equal(S2[[0, 1, 2, 4, 5]], 2 * S[[0, 1, 2, 4, 5]])
+    # the scale is the correctly rounded fp32 quotient amax / 448, bit for bit
+    # (numpy's float32 division is IEEE), on rows of many magnitudes
+    Wm = (rng.standard_normal((64, 33)) * np.exp(rng.uniform(-12, 12, (64, 1)))).astype(np.float32)
+    _, Sm = orc.quantize_rows_fp8(Wm)
+    want = np.abs(Wm).max(axis=1).astype(np.float32) / np.float32(448.0)
+    assert want.dtype == np.float32
+    assert np.array_equal(Sm.view(np.uint32), want.view(np.uint32))
+    # The code is decided by the fp32 quotient W / s.  A hand-built row whose
+    # fp32 quotient lands exactly on an e4m3 tie while the exact quotient lies
+    # just above it: amax = 1 + 2^-20, s = fl32(amax / 448) = 0x1.24925cp-9,
+    # w = 0x1.36db82p-9.  w / s = 1.0625 + 1.3e-8 exactly; the nearest fp32 is
+    # 1.0625, the tie between the e4m3 values 1 (significand 1.000) and 1.125
+    # (1.001), which rounds to the even one, 1.  The exact quotient would give
+    # 1.125.
+    amax, w = np.float32(1 + 2.0 ** -20), np.float32(float.fromhex("0x1.36db82p-9"))
+    s32 = amax / np.float32(448.0)
+    assert float(s32) == float.fromhex("0x1.24925cp-9")
+    assert float(w / s32) == 1.0625 and float(w) / float(s32) > 1.0625   # the fixture itself
+    Qt, St = orc.quantize_rows_fp8(np.array([[amax, w, -w]], np.float32))
+    assert St[0] == s32
+    assert Qt[0, 1] == 1.0 and Qt[0, 2] == -1.0, Qt
     # FP8 column split (none / GELU / SwiGLU) against numpy on the dequantized weight
     X = rng.standard_normal((3, 40)).astype(np.float32)
     b = rng.standard_normal(6).astype(np.float32)

@@ -47,6 +47,15 @@ MUTANTS = [
     ("ring_partial_not_rounded",
      "for (int64_t e = 0; e < L; ++e) pi[e] = wire_bf16 ? orc_round_bf16(pi[e]) : orc_round_f32(pi[e]);",
      ";"),
+    # the fp32 wire of the ring kept in fp64
+    ("round_f32_identity", "double orc_round_f32(double x) { return (double)(float)x; }",
+     "double orc_round_f32(double x) { return x; }"),
+    # the FP8 quotient W / s taken in fp64 instead of fp32
+    ("fp8_quotient_fp64", "const float v = W[r * ldw + c] / sc; /* fp32 division */",
+     "const double v = (double)W[r * ldw + c] / (double)sc;"),
+    # the FP8 row scale one fp32 ulp off
+    ("fp8_scale_one_ulp", "const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;",
+     "const float sc = amax > 0.0f ? nextafterf(amax / 448.0f, 1e30f) : 1.0f;"),
 ]
 
 
