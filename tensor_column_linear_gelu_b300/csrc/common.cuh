@@ -19,8 +19,12 @@ __device__ __forceinline__ float act_gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752440f));
 }
 
-// SiLU: z * sigmoid(z) = z / (1 + e^-z).
-__device__ __forceinline__ float act_silu(float z) { return z / (1.0f + expf(-z)); }
+// SiLU: z * sigmoid(z) = z / (1 + e^-z).  The quotient uses the
+// approximate division (within 2 ulp; a denominator of 2^126 or more, which
+// only z < -87 produces, gives the limit 0): the IEEE-rounded division
+// branches to a slow path for such denominators, and that branch serialised
+// the decode kernel's single epilogue warp.
+__device__ __forceinline__ float act_silu(float z) { return __fdividef(z, 1.0f + expf(-z)); }
 
 // ---------------------------------------------------------------- bf16 bits
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }

@@ -458,25 +458,32 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
         tc_fence_after();
         const uint32_t taddr =
             tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.acc_stride);
+        // Only lanes t < M hold a token; the other lanes' accumulator rows
+        // come from shared memory that is not this call's X (whatever the
+        // ring held), so they only take part in the warp-collective TMEM
+        // loads: no arithmetic and no stores.  Accumulator columns are read
+        // 16 (gate and up: 2 x 16) at a time with one wait.
+        const bool live = t < p.M;
         if (has_tokens && p.row && p.cs > 1) {
           // this rank's partial sum -> shared memory, for the cluster reduction
           const int c = tl.pc[0].c;
 #pragma unroll 1
-          for (int j0 = 0; j0 < c; j0 += 8) {
-            float v[8];
-            tmem_ld8(taddr + (uint32_t)j0, v);
-            if (F8) {
-              // this CTA's partial belongs to shard rshard: its row scales
-              const float* sc = p.wscale[rshard] + tl.pc[0].loc + j0;
+          for (int j0 = 0; j0 < c; j0 += 16) {
+            float v[16];
+            tmem_ld16(taddr + (uint32_t)j0, v);
+            if (live &&
+                TP_CHECK(p.err, (int64_t)(t * SK_RED_PITCH + j0 + 16) * 4 <= p.ring_bytes)) {
+              if (F8) {
+                // this CTA's partial belongs to shard rshard: its row scales
+                const float* sc = p.wscale[rshard] + tl.pc[0].loc + j0;
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                if (j0 + j < c) v[j] *= __ldg(sc + j);
-            }
-            if (t < p.M &&
-                TP_CHECK(p.err, (int64_t)(t * SK_RED_PITCH + j0 + 8) * 4 <= p.ring_bytes)) {
+                for (int j = 0; j < 16; ++j)
+                  if (j0 + j < c) v[j] *= __ldg(sc + j);
+              }
               float4* dst = reinterpret_cast<float4*>(red + t * SK_RED_PITCH + j0);
-              dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-              dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
           }
         } else if (has_tokens) {
@@ -489,38 +496,53 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
             if (F8)
               sc = p.wscale[p.row ? rshard : pc.shard] +
                    (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G : pc.loc);
+            // 16 columns per step (8 in FP8 mode, whose 704 threads leave
+            // fewer registers each)
+            constexpr int CH = F8 ? 8 : 16;
 #pragma unroll 1
-            for (int j0 = 0; j0 < pc.c; j0 += 8) {
-              float v[8];
-              tmem_ld8(taddr + (uint32_t)(pc.slot + j0), v);
-              const int valid = pc.c - j0 < 8 ? pc.c - j0 : 8;
+            for (int j0 = 0; j0 < pc.c; j0 += CH) {
+              // columns [slot + j0, slot + j0 + CH) lie inside the piece's
+              // slot (slots are multiples of 16 wide)
+              float v[CH], u[CH];
+              const uint32_t tg = taddr + (uint32_t)(pc.slot + j0);
+              const uint32_t tu = taddr + (uint32_t)(tl.rows + pc.slot + j0);
+              if constexpr (CH == 16) {
+                if (swiglu)
+                  tmem_ld16x2(tg, tu, v, u);
+                else
+                  tmem_ld16(tg, v);
+              } else {
+                tmem_ld8(tg, v);
+                if (swiglu) tmem_ld8(tu, u);
+              }
+              if (!live) continue;
+              const int valid = pc.c - j0 < CH ? pc.c - j0 : CH;
               if (F8) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  if (j < valid) v[j] *= __ldg(sc + j0 + j);
+                for (int j = 0; j < CH; ++j)
+                  if (j < valid) {
+                    v[j] *= __ldg(sc + j0 + j);
+                    if (swiglu) u[j] *= __ldg(sc + G + j0 + j);
+                  }
               }
               if (swiglu) {
-                float u[8];
-                tmem_ld8(taddr + (uint32_t)(tl.rows + pc.slot + j0), u);
-                if (F8) {
 #pragma unroll
-                  for (int j = 0; j < 8; ++j)
-                    if (j < valid) u[j] *= __ldg(sc + G + j0 + j);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = act_silu(v[j]) * u[j];
+                for (int j = 0; j < CH; ++j) v[j] = act_silu(v[j]) * u[j];
               } else {
                 if (bias) {
 #pragma unroll
-                  for (int j = 0; j < 8; ++j)
+                  for (int j = 0; j < CH; ++j)
                     if (j < valid) v[j] += __ldg(bias + pc.loc + j0 + j);
                 }
                 if (!p.row && p.act == TP_ACT_GELU_ERF) {
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) v[j] = act_gelu_erf(v[j]);
+                  for (int j = 0; j < CH; ++j) v[j] = act_gelu_erf(v[j]);
                 }
               }
-              if (t < p.M) store_row8(p.Y, p.ydt, base, pc.loc + j0, valid, v);
+              if constexpr (CH == 16)
+                store_row16(p.Y, p.ydt, base, pc.loc + j0, valid, v);
+              else
+                store_row8(p.Y, p.ydt, base, pc.loc + j0, valid, v);
             }
           }
         }

@@ -110,6 +110,31 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns at each of two TMEM addresses of this thread's
+// lane (a SwiGLU output's gate and up accumulators), with one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16],
+                                            float (&b)[16]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[16 + i]);
+  }
+}
+
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -174,6 +199,11 @@ __device__ __forceinline__ void store_row32(void* Y, int ydt, int64_t base, int6
     }
   }
 }
+
+// 16 consecutive outputs v[0..15] of one row at columns n0.. (n0 + 15), of
+// which the first `valid` exist: two 8-wide stores.
+__device__ __forceinline__ void store_row16(void* Y, int ydt, int64_t base, int64_t n0,
+                                            int valid, const float (&v)[16]);
 
 // 8 consecutive outputs v[0..7] of one row at columns n0.. (n0 + 7), of which
 // the first `valid` exist.  One vector store when the address allows.
@@ -341,6 +371,18 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtens
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ void store_row16(void* Y, int ydt, int64_t base, int64_t n0,
+                                            int valid, const float (&v)[16]) {
+  float lo[8], hi[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    lo[j] = v[j];
+    hi[j] = v[8 + j];
+  }
+  store_row8(Y, ydt, base, n0, valid < 8 ? valid : 8, lo);
+  if (valid > 8) store_row8(Y, ydt, base, n0 + 8, valid - 8, hi);
 }
 
 }  // namespace tpla
