@@ -79,6 +79,9 @@ def _bind(lib):
                                      _i64, _f, _d, _i64]
     lib.orc_row_parallel_ring.argtypes = [ctypes.c_int, _i64, _i64, _i64, _f, _i64, _f,
                                           _i64, _f, ctypes.c_int, _d, _i64]
+    lib.orc_row_parallel_ring_rows.argtypes = [ctypes.c_int, _i64, ctypes.POINTER(_i64), _i64,
+                                               _i64, _i64, _f, _i64, _f, _i64, _f, ctypes.c_int,
+                                               _d, _i64]
     lib.orc_quantize_fp8_rows.argtypes = [_i64, _i64, _f, _i64, _f, _f]
     lib.orc_column_parallel_fp8.argtypes = [ctypes.c_int, _i64, _i64, _i64, _f, _i64, _f, _f,
                                             _i64, _f, _f, _f, ctypes.c_int, _d, _i64]
@@ -92,6 +95,7 @@ def _bind(lib):
                                _f, _f, _f, _d]
     for name in ("orc_linear", "orc_swiglu", "orc_column_parallel",
                  "orc_column_parallel_uneven", "orc_row_parallel", "orc_row_parallel_ring",
+                 "orc_row_parallel_ring_rows",
                  "orc_quantize_fp8_rows", "orc_column_parallel_fp8", "orc_row_parallel_fp8",
                  "orc_mlp_block",
                  "orc_qkv_proj", "orc_o_proj"):
@@ -215,6 +219,22 @@ class Oracle:
         _check(self._lib.orc_row_parallel_ring(tp, M, K, N, _pf(X), K, _pf(W), K, _pf(b),
                                                1 if wire == "bf16" else 0, _pd(Y), N),
                "row_parallel_ring")
+        return Y
+
+    def row_parallel_ring_rows(self, tp, M_total, rows, X, W, b=None, wire="bf16"):
+        """row_parallel_ring on some rows of a call of M_total rows: X holds the
+        sampled input rows, rows[r] their row numbers in the full call; the
+        chunks of the ring are those of the full [M_total, N] message."""
+        X, W, b = _f32(X), _f32(W), _f32(b)
+        n, K = X.shape
+        N = W.shape[0]
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        assert W.shape[1] == K and r.shape == (n,) and wire in ("bf16", "f32")
+        Y = np.empty((n, N), dtype=np.float64)
+        _check(self._lib.orc_row_parallel_ring_rows(tp, M_total, r.ctypes.data_as(ctypes.POINTER(_i64)),
+                                                    n, K, N, _pf(X), K, _pf(W), K, _pf(b),
+                                                    1 if wire == "bf16" else 0, _pd(Y), N),
+               "row_parallel_ring_rows")
         return Y
 
     # ------------------------------------------------------------ FP8 weights

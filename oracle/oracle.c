@@ -327,6 +327,50 @@ int orc_row_parallel_ring(int tp, int64_t M, int64_t K, int64_t N, const float* 
   return ORC_OK;
 }
 
+/*
+ * The same ring-ordered all-reduce, evaluated only on some rows of a call of
+ * M_total rows: X holds the n_rows sampled input rows, rows[r] is the row
+ * number of sampled row r in the full call, and Y receives those output
+ * rows.  The chunks are those of the full call's flattened [M_total, N]
+ * message, so element (rows[r], n) is summed exactly as orc_row_parallel_ring
+ * sums it in the full call; each element is computed on its own (its
+ * partials, its chunk's start rank, the hops in ring order).
+ */
+int orc_row_parallel_ring_rows(int tp, int64_t M_total, const int64_t* rows, int64_t n_rows,
+                               int64_t K, int64_t N, const float* X, int64_t ldx,
+                               const float* W, int64_t ldw, const float* b, int wire_bf16,
+                               double* Y, int64_t ldy) {
+  if (tp < 1 || tp > 64) return ORC_ERR_BAD_SHAPE;
+  if (M_total < 0 || n_rows < 0 || K < 0 || N < 0) return ORC_ERR_BAD_SHAPE;
+  if (K % tp != 0) return ORC_ERR_NOT_DIVISIBLE;
+  if (n_rows > 0 && !rows) return ORC_ERR_NULL;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= M_total) return ORC_ERR_BAD_SHAPE;
+  const int64_t ks = K / tp;
+  const int64_t L = M_total * N;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t r = 0; r < n_rows; ++r)
+    for (int64_t n = 0; n < N; ++n) {
+      double p[64];
+      /* rank i's partial for this element, held in the wire dtype */
+      for (int i = 0; i < tp; ++i) {
+        const double v = dot(ks, X + r * ldx + (int64_t)i * ks, W + n * ldw + (int64_t)i * ks);
+        p[i] = wire_bf16 ? orc_round_bf16(v) : orc_round_f32(v);
+      }
+      /* the chunk holding flattened element e of the full message */
+      const int64_t e = rows[r] * N + n;
+      int c = 0;
+      while (c + 1 < tp && (int64_t)(c + 1) * L / tp <= e) ++c;
+      double acc = p[c];
+      for (int s = 1; s < tp; ++s) {
+        acc += p[(c + s) % tp];
+        acc = wire_bf16 ? orc_round_bf16(acc) : orc_round_f32(acc);
+      }
+      Y[r * ldy + n] = acc + (b ? (double)b[n] : 0.0);
+    }
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* FP8 (e4m3) weights with one fp32 scale per weight row                     */
 /* ------------------------------------------------------------------------ */

@@ -311,6 +311,23 @@ def check_ring_allreduce(orc):
     W = np.tile(np.array([[t24, 1, 1, 1]], np.float32), (2, 1))
     y = orc.row_parallel_ring(2, X, W, None, "f32")
     assert np.array_equal(y, [[t24 + 2, t24 + 2]]), y
+    # The sampled-rows form keeps the full call's chunks.  Case A with M=2:
+    # L = 10 splits into [0,3), [3,6), [6,10).  Row 1 is elements 5..9:
+    # element 5 lies in chunk 1 (starts at rank 1: 1+1=2, +256 = 258),
+    # elements 6..9 in chunk 2 (starts at rank 2: 1+256=257 -> 256, +1 -> 256).
+    X = np.ones((1, 3), np.float32)
+    W = np.tile(np.array([[256, 1, 1]], np.float32), (5, 1))
+    y = orc.row_parallel_ring_rows(3, 2, [1], X, W, None, "bf16")
+    assert np.array_equal(y, [[258, 256, 256, 256, 256]]), y
+    # and every sampled row equals that row of the full call
+    Xf = rng.standard_normal((9, 48)).astype(np.float32) * 40
+    Wf = rng.standard_normal((7, 48)).astype(np.float32)
+    bf = rng.standard_normal(7).astype(np.float32)
+    for tp, wire in ((3, "bf16"), (4, "f32"), (2, "bf16")):
+        full = orc.row_parallel_ring(tp, Xf, Wf, bf, wire)
+        rows = [0, 3, 4, 8]
+        assert np.array_equal(orc.row_parallel_ring_rows(tp, 9, rows, Xf[rows], Wf, bf, wire),
+                              full[rows])
     # fp32 wire: within a few fp32 roundings of the exact sum
     X = rng.standard_normal((4, 96)).astype(np.float32)
     W = rng.standard_normal((7, 96)).astype(np.float32)

@@ -56,6 +56,11 @@ MUTANTS = [
     # the FP8 row scale one fp32 ulp off
     ("fp8_scale_one_ulp", "const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;",
      "const float sc = amax > 0.0f ? nextafterf(amax / 448.0f, 1e30f) : 1.0f;"),
+    # the sampled-rows ring: chunk of the sampled row's own index, not the full call's
+    ("ring_rows_local_chunk", "const int64_t e = rows[r] * N + n;", "const int64_t e = r * N + n;"),
+    ("ring_rows_no_hop_rounding",
+     "        acc += p[(c + s) % tp];\n        acc = wire_bf16 ? orc_round_bf16(acc) : orc_round_f32(acc);",
+     "        acc += p[(c + s) % tp];"),
 ]
 
 
