@@ -24,6 +24,9 @@ from tensor_column_linear_gelu_b300 import tpla
 
 TOL_F32 = 1e-5
 TOL_BF16_RMS = 5e-3
+# unit roundoff of the wire dtypes of the ring-ordered shard sum
+U_BF16 = 2.0 ** -8
+U_F32 = 2.0 ** -24
 
 
 def np64(t: torch.Tensor) -> np.ndarray:

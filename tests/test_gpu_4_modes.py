@@ -17,13 +17,13 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import (assert_bf16_is_rounded_fp32, assert_bitwise_equal, assert_close_bf16,
-                         assert_close_fp32, assert_h_bf16, np64, shard)
+from gpu_helpers import (U_BF16, U_F32, assert_bf16_is_rounded_fp32, assert_bitwise_equal,
+                         assert_close_bf16, assert_close_fp32, assert_h_bf16, np64, shard)
 from tensor_column_linear_gelu_b300 import inputs, tpla
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-U = {torch.bfloat16: 2.0 ** -8, torch.float32: 2.0 ** -24}
+U = {torch.bfloat16: U_BF16, torch.float32: U_F32}
 
 
 @pytest.fixture(scope="module", autouse=True)
