@@ -492,8 +492,10 @@ tp_status tp_layer_forward(const tp_layer_args* args, tp_stream_t stream);
  *   Limit       M * d_ff * (2 for TP_BF16, 4 for TP_F32) <= TP_NOALLOC_SCRATCH_BYTES,
  *               e.g. up to 146 tokens at d_ff = 28672 in bf16.  Larger calls
  *               return TP_ERR_UNSUPPORTED and launch nothing.
- *   Set-up      the first call on a device looks up the buffer's device
- *               address (with that device current).  Make that first call
+ *   Set-up      every call looks up the buffer's device address on the
+ *               current device (nothing is cached, so a device reset leaves
+ *               no stale address behind).  The first call on a device may
+ *               load the library's device code there: make that first call
  *               before any stream capture on the device.
  *   Sharing     every call on a device uses the same buffer, which keeps the
  *               last call's contents.  Nothing in it needs to start at zero:

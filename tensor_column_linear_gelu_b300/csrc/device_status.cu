@@ -4,6 +4,8 @@
 // Kernels with spin-waits take the word's device address as a parameter and
 // atomically OR a code into it when a bounded wait gives up (see sync.cuh).
 // tp_device_status() synchronises the caller's stream, reads and clears it.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "sync.cuh"
@@ -31,10 +33,15 @@ __global__ void bounded_wait_selftest_kernel(unsigned int* err, uint64_t limit_n
 
 }  // namespace
 
+// Device address of the error word on the current device.  Cached per
+// device; the cache is guarded, so concurrent first calls from several host
+// threads are safe.
 unsigned int* device_error_word() {
   static unsigned int* cache[64] = {nullptr};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   if (!cache[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;

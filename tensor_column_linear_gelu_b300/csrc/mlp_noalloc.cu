@@ -10,7 +10,6 @@
 // that is part of the library image: every GPU that loads the library holds
 // it until the process exits.  This call allocates nothing.
 #include <cstdint>
-#include <mutex>
 
 #include "internal.h"
 
@@ -22,26 +21,19 @@ namespace {
 // device address that scratch_address() looks up instead.
 static __device__ __align__(256) unsigned char g_mlp_scratch[TP_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_mlp_scratch on the current device.  Looked up once per
-// device (with that device current) on the first call, then cached.
+// Device address of g_mlp_scratch on the current device, looked up on every
+// call with that device current (a cheap host query).  Nothing is cached, so
+// an address can never outlive the context it belongs to (a device reset, a
+// context torn down and re-created).  The very first lookup on a device may
+// load the library's device code there; that first call must come before any
+// stream capture on the device.
 void* scratch_address(tp_status* status) {
-  static void* cache[64] = {nullptr};
-  static std::mutex mu;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_mlp_scratch) != cudaSuccess || p == nullptr) {
     *status = TP_ERR_CUDA;
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_mlp_scratch) != cudaSuccess || p == nullptr) {
-      *status = TP_ERR_CUDA;
-      return nullptr;
-    }
-    cache[dev] = p;
-  }
-  return cache[dev];
+  return p;
 }
 
 }  // namespace

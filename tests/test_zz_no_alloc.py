@@ -5,17 +5,23 @@ plugin whose host hands out no device memory, a path where cudaMalloc's
 implicit synchronisation is not allowed) cannot provide tp_mlp_block's [M, d_ff]
 workspace; this entry point keeps that workspace in a fixed buffer built into
 the library.  Each test calls it twice in a row through the C ABI and checks
-both results against tp_mlp_block on the same inputs, with the tolerance used
-by every bf16 parity test (5e-3 x RMS).  This file is collected last so that a
-run stopping at its first failure has already run every other test; it needs
-nothing from them and also passes alone in a fresh process.
+both results against tp_mlp_block on the same inputs: the two run the same
+kernels in the same order, so the outputs must be bit-identical.  The first
+result is also checked against the fp64 oracle with the tolerances of every
+parity test (bf16 inputs: 5e-3 x RMS; fp32 inputs: 1e-5 x (|y| + 1)).  The
+cases reach every kernel family with h in the fixed buffer: the
+weight-streaming GEMV (one token, and the fp32 path), the tensor-core decode
+kernel (3..128 tokens) and the prefill GEMM on CTA pairs (more than 128
+tokens), all within the buffer's 8 MiB.  This file is collected last so that
+a run stopping at its first failure has already run every other test; it
+needs nothing from them and also passes alone in a fresh process.
 """
 import ctypes
 
 import pytest
 import torch
 
-from gpu_helpers import assert_close_bf16, np64
+from gpu_helpers import assert_bitwise_equal, assert_close_bf16, assert_close_fp32
 from tensor_column_linear_gelu_b300 import inputs, tpla
 
 pytestmark = pytest.mark.gpu
@@ -38,27 +44,41 @@ def _noalloc_abi(tp, X, w1, b1, w2, b2, act, d_ff, Y):
         tpla.stream_handle(None))
 
 
-# M, d_model, d_ff, tp, act: a decode shape (weight-streaming kernels) and a
-# shape on the tensor-core kernels, both within the built-in 8 MiB workspace.
-CASES = [(4, 256, 1024, 4, "swiglu"), (96, 512, 2048, 2, "gelu")]
+# M, d_model, d_ff, tp, act, input dtype; h = M * d_ff elements of the input
+# dtype, at most 2 MiB here (the buffer holds 8 MiB)
+CASES = [
+    (1, 256, 1024, 4, "swiglu", torch.bfloat16),   # weight-streaming GEMV
+    (3, 256, 512, 2, "gelu", torch.float32),       # fp32 path (GEMV), h in fp32
+    (4, 256, 1024, 4, "swiglu", torch.bfloat16),   # tensor-core decode kernel
+    (96, 512, 2048, 2, "gelu", torch.bfloat16),    # tensor-core decode kernel
+    (512, 512, 2048, 2, "gelu", torch.bfloat16),   # prefill GEMM on CTA pairs
+]
 
 
-@pytest.mark.parametrize("M,d,dff,tp,act", CASES)
-def test_noalloc_matches_tp_mlp_block_twice(M, d, dff, tp, act):
+@pytest.mark.parametrize("M,d,dff,tp,act,dt", CASES)
+def test_noalloc_matches_tp_mlp_block_twice(orc, M, d, dff, tp, act, dt):
     bias = act != "swiglu"
-    f = inputs.ffn(seed=500 + M, M=M, d_model=d, d_ff=dff, act=act, bias=bias, device=DEV)
+    f = inputs.ffn(seed=500 + M, M=M, d_model=d, d_ff=dff, act=act, bias=bias, device=DEV,
+                   dtype=dt)
     split = "gate_up" if act == "swiglu" else "column"
     w1, b1 = tpla.tp_shard_weights(split, tp, f.W1, W_up=f.W_up, b=f.b1)
     w2, _ = tpla.tp_shard_weights("row", tp, f.W2)
-    X2 = inputs.normal((M, d), 1.0, 900 + M, torch.bfloat16, DEV)   # second call: new tokens
-    for X in (f.X, X2):
+    X2 = inputs.normal((M, d), 1.0, 900 + M, dt, DEV)   # second call: new tokens
+    for k, X in enumerate((f.X, X2)):
         ref, _ = tpla.tp_mlp_block(tp, X, w1, b1, w2, f.b2, act, d_ff=dff,
                                    out_dtype=torch.float32)
         Y = torch.full((M, d), float("nan"), dtype=torch.float32, device=DEV)
         st = _noalloc_abi(tp, X, w1, b1, w2, f.b2, act, dff, Y)
         assert st == tpla.TP_OK, tpla.status_string(st)
         torch.cuda.synchronize()
-        assert_close_bf16(Y, np64(ref))
+        assert_bitwise_equal(Y, ref, f"call {k + 1}: noalloc vs tp_mlp_block")
+        if k == 0:
+            y_ref, _ = orc.mlp_block(tp, X, f.W1, f.b1, f.W2, f.b2, act, W1u=f.W_up,
+                                     round_h=(dt == torch.bfloat16))
+            if dt == torch.bfloat16:
+                assert_close_bf16(Y, y_ref)
+            else:
+                assert_close_fp32(Y, y_ref)
     assert tpla.tp_device_status() == tpla.TP_OK
 
 
