@@ -6,10 +6,32 @@
 // same summation order whatever the shard count.
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include "internal.h"
 
 namespace tpla {
+
+tp_status fire(const Launch& L, cudaStream_t stream) {
+  if (!L.kernel) return TP_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = L.grid;
+  cfg.blockDim = L.block;
+  cfg.dynamicSmemBytes = L.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (L.cluster > 0) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = L.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {const_cast<unsigned char*>(L.params)};
+  if (cudaLaunchKernelExC(&cfg, L.kernel, args) != cudaSuccess) return TP_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
 
 int sm_count() {
   static int cache[64] = {0};
@@ -68,7 +90,8 @@ tp_status check_bias_array(const float* const* b, int tp) {
   return TP_OK;
 }
 
-// The one place a validated problem picks its kernel.  The choice depends on
+// The one place a validated problem picks its kernel, and prepares its launch
+// (launching nothing).  The choice depends on
 // the dtype and the token count M only (never on N or tp):
 //   fp32, or bf16 with M <= kGemvMaxTokens      weight-streaming GEMV (CUDA cores)
 //   bf16, kGemvMaxTokens < M <= kSkinnyMaxTokens  tcgen05 decode kernel
@@ -78,19 +101,45 @@ tp_status check_bias_array(const float* const* b, int tp) {
 //   FP8 weights, larger M                         tcgen05 decode kernel, FP8 mode
 // (FP8 row-parallel calls with tp above the decode kernels' largest cluster
 // also take the FP8 GEMV: their CTAs must each hold one shard's k-range.)
-tp_status run(const LinearProblem& p, cudaStream_t s) {
+tp_status prepare(const LinearProblem& p, Launch* L) {
+  L->kernel = nullptr;
   if (p.M == 0) return TP_OK;
   if (p.fp8) {
     if (p.M <= kGemvMaxTokens || (p.row && p.tp > kSkinnyMaxCluster))
-      return launch_gemv_fp8(p, s);
-    if (p.M <= kFp8TmemMaxTokens) return launch_decode_fp8(p, s);
-    return launch_skinny(p, s);
+      return prepare_gemv_fp8(p, L);
+    if (p.M <= kFp8TmemMaxTokens) return prepare_decode_fp8(p, L);
+    return prepare_skinny(p, L);
   }
   if (p.xdt == TP_BF16 && p.M > kGemvMaxTokens) {
-    if (p.M <= kSkinnyMaxTokens) return launch_skinny(p, s);
-    return launch_gemm_pair(p, s);
+    if (p.M <= kSkinnyMaxTokens) return prepare_skinny(p, L);
+    return prepare_gemm_pair(p, L);
   }
-  return launch_gemv(p, s);
+  return prepare_gemv(p, L);
+}
+
+tp_status run(const LinearProblem& p, cudaStream_t s) {
+  Launch L;
+  tp_status st = prepare(p, &L);
+  if (st != TP_OK) return st;
+  return fire(L, s);
+}
+
+// Prepare every problem of a call, then launch them in order: a host-side
+// failure (a tensor map that cannot be encoded, a shape no kernel offers) is
+// reported before anything runs, so the call writes nothing.  Only a launch
+// that CUDA itself rejects can stop the sequence part-way (TP_ERR_CUDA).
+tp_status run_seq(const LinearProblem* const* ps, int n, cudaStream_t s) {
+  thread_local std::vector<Launch> launches;
+  if ((int)launches.size() < n) launches.resize((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    const tp_status st = prepare(*ps[i], &launches[(size_t)i]);
+    if (st != TP_OK) return st;
+  }
+  for (int i = 0; i < n; ++i) {
+    const tp_status st = fire(launches[(size_t)i], s);
+    if (st != TP_OK) return st;
+  }
+  return TP_OK;
 }
 
 LinearProblem column_problem(int tp, int64_t M, int64_t K, int64_t N, const void* X,
@@ -385,13 +434,15 @@ tp_status row_parallel_linear_ring(int tp, int64_t M, int64_t K, int64_t N, cons
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // rank i's local partial X_i . W_i^T, rounded once to the wire dtype
   const int64_t L = M * N;
+  LinearProblem parts[TP_MAX_TP];
+  const LinearProblem* seq[TP_MAX_TP];
   for (int i = 0; i < tp; ++i) {
     const void* xi = static_cast<const char*>(X) + (int64_t)i * ks * es;
     void* pi = static_cast<char*>(partials) + (int64_t)i * L * esz(wire_dt);
-    LinearProblem p = row_problem(1, M, ks, N, xi, ldx, xdt, &w_shards[i], nullptr, pi, N,
-                                  wire_dt);
-    if ((st = run(p, s)) != TP_OK) return st;
+    parts[i] = row_problem(1, M, ks, N, xi, ldx, xdt, &w_shards[i], nullptr, pi, N, wire_dt);
+    seq[i] = &parts[i];
   }
+  if ((st = run_seq(seq, tp, s)) != TP_OK) return st;
   return launch_ring_reduce(tp, M, N, partials, wire_dt, b, Y, ldy, ydt, s);
 }
 
@@ -475,16 +526,18 @@ tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M
     return run(p, s);
   }
   int64_t off = 0;
+  LinearProblem parts[TP_MAX_TP];
+  const LinearProblem* seq[TP_MAX_TP];
   for (int i = 0; i < tp; ++i) {
     // many tokens: shard i as a one-shard call writing columns [off, off +
     // widths[i]) of Y -- the prefill GEMM's tiles need an equal split
     void* yi = static_cast<char*>(Y) + off * esz(ydt);
-    LinearProblem p = column_problem(1, M, K, widths[i], X, ldx, xdt, &w_shards[i],
-                                     b_shards ? &b_shards[i] : nullptr, act, yi, ldy, ydt, 0);
-    if ((st = run(p, s)) != TP_OK) return st;
+    parts[i] = column_problem(1, M, K, widths[i], X, ldx, xdt, &w_shards[i],
+                              b_shards ? &b_shards[i] : nullptr, act, yi, ldy, ydt, 0);
+    seq[i] = &parts[i];
     off += widths[i];
   }
-  return TP_OK;
+  return run_seq(seq, tp, s);
 }
 
 tp_status tp_quantize_fp8(int64_t rows, int64_t cols, const void* W, void* Q, float* scales,
@@ -588,8 +641,8 @@ tp_status tp_mlp_block_fp8(int tp, int64_t M, int64_t d_model, int64_t d_ff, tp_
     up.wscale[i] = s1_shards[i];
     down.wscale[i] = s2_shards[i];
   }
-  if ((st = run(up, s)) != TP_OK) return st;
-  return run(down, s);
+  const LinearProblem* seq[2] = {&up, &down};
+  return run_seq(seq, 2, s);
 }
 
 tp_status tp_mlp_block(int tp, int64_t M, int64_t d_model, int64_t d_ff, tp_act act, tp_dtype xdt,
@@ -601,9 +654,8 @@ tp_status tp_mlp_block(int tp, int64_t M, int64_t d_model, int64_t d_ff, tp_act 
   tp_status st = prepare_mlp(tp, M, d_model, d_ff, act, xdt, X, w1_shards, b1_shards, w2_shards,
                              b2, h, Y, ydt, &up, &down, &empty);
   if (st != TP_OK || empty) return st;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = run(up, s)) != TP_OK) return st;
-  return run(down, s);
+  const LinearProblem* seq[2] = {&up, &down};
+  return run_seq(seq, 2, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads, int n_kv_heads,
@@ -617,9 +669,8 @@ tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads, int n_kv
                               bqkv_shards, qkv_out, qkv_dt, ctx, wo_shards, bo, Y, ydt, &qkv, &o,
                               &empty);
   if (st != TP_OK || empty) return st;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = run(qkv, s)) != TP_OK) return st;
-  return run(o, s);
+  const LinearProblem* seq[2] = {&qkv, &o};
+  return run_seq(seq, 2, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_layer_forward(const tp_layer_args* a, tp_stream_t stream) {
@@ -639,11 +690,8 @@ tp_status tp_layer_forward(const tp_layer_args* a, tp_stream_t stream) {
   // then that output must be in the input dtype.
   TP_RET_IF(a->X_ffn == a->Y_attn && a->attn_ydt != a->xdt, TP_ERR_DTYPE);
   if (empty_attn) return TP_OK;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = run(qkv, s)) != TP_OK) return st;
-  if ((st = run(o, s)) != TP_OK) return st;
-  if ((st = run(up, s)) != TP_OK) return st;
-  return run(down, s);
+  const LinearProblem* seq[4] = {&qkv, &o, &up, &down};
+  return run_seq(seq, 4, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_device_status(tp_stream_t stream) {

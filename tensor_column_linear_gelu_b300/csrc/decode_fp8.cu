@@ -105,6 +105,7 @@ struct Fp8TmemParams {
   const float* bias[TP_MAX_TP];
   const float* wscale[TP_MAX_TP];  // scale of each row of W_i
   void* Y;
+  int64_t y_extent;  // elements of Y this call may write (checked builds)
   unsigned int* err;
   int64_t ldy;
   int64_t fo[TP_MAX_TP + 1];     // column: shard i owns features [fo[i], fo[i+1])
@@ -430,10 +431,9 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
                 if (p.row && p.cs > 1) {
                   if (TP_CHECK(p.err, (t * TF_RED_PITCH + s + 1) * 4 <= p.ring_bytes))
                     red[t * TF_RED_PITCH + s] = v[j];  // this rank's partial, slot = output
-                } else if (p.row) {
-                  store_out(p.Y, p.ydt, t * p.ldy + n, v[j]);
                 } else {
-                  store_out(p.Y, p.ydt, p.yoff[pc.shard] + t * p.ldy + n, v[j]);
+                  const int64_t e = (p.row ? 0 : p.yoff[pc.shard]) + t * p.ldy + n;
+                  if (TP_CHECK(p.err, e < p.y_extent)) store_out(p.Y, p.ydt, e, v[j]);
                 }
               }
             }
@@ -539,7 +539,8 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
         float sum = 0.0f;
         for (int r = 0; r < p.cs; ++r) sum += dsmem_ld_f32(dsmem_addr(red_s + off, (uint32_t)r));
         if (bias) sum += __ldg(bias + loc + j);
-        store_out(p.Y, p.ydt, tok * p.ldy + loc + j, sum);
+        if (TP_CHECK(p.err, tok * p.ldy + loc + j < p.y_extent))
+          store_out(p.Y, p.ydt, tok * p.ldy + loc + j, sum);
       }
     }
     cluster_sync_all();  // no CTA leaves while a peer still reads its buffer
@@ -555,7 +556,7 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
 
 }  // namespace
 
-tp_status launch_decode_fp8(const LinearProblem& p, cudaStream_t stream) {
+tp_status prepare_decode_fp8(const LinearProblem& p, Launch* L) {
   if (!p.fp8 || p.xdt != TP_BF16 || p.M < 1 || p.M > kFp8TmemMaxTokens) return TP_ERR_UNSUPPORTED;
   if (p.row && p.tp > TF_MAX_CLUSTER) return TP_ERR_UNSUPPORTED;
   Fp8TmemParams fp{};
@@ -588,6 +589,7 @@ tp_status launch_decode_fp8(const LinearProblem& p, cudaStream_t stream) {
   }
   fp.Y = p.Y;
   fp.ldy = p.ldy;
+  fp.y_extent = output_extent(p);
   for (int i = 0; i <= p.tp; ++i) fp.fo[i] = p.fo[i];
   for (int i = 0; i < p.tp; ++i) fp.yoff[i] = p.yoff[i];
   fp.M = p.M;
@@ -647,20 +649,13 @@ tp_status launch_decode_fp8(const LinearProblem& p, cudaStream_t stream) {
                                     TF_SMEM_MAX);
   });
   if (attr_err != cudaSuccess) return TP_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(TF_THREADS);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)fp.cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, fp8_tmem_kernel, fp) != cudaSuccess) return TP_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  L->kernel = reinterpret_cast<const void*>(fp8_tmem_kernel);
+  L->grid = dim3((unsigned)grid);
+  L->block = dim3(TF_THREADS);
+  L->smem = (size_t)smem;
+  L->cluster = (unsigned)fp.cs;
+  L->set_params(fp);
+  return TP_OK;
 }
 
 }  // namespace tpla

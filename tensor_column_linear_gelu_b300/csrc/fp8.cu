@@ -80,6 +80,7 @@ struct Fp8Params {
   void* Y;
   int64_t wrows[TP_MAX_TP];    // rows of each code buffer (checked builds)
   unsigned int* err;           // device error word (checked builds)
+  int64_t y_extent;            // elements of Y this call may write (checked builds)
 };
 
 __device__ __forceinline__ void fp8x16_to_float(const uint4& v, float (&f)[16]) {
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constan
           if constexpr (ROW) {
             float z = acc[mm][r];
             if (p.bias[0]) z += p.bias[0][o];
-            store_out(p.Y, p.ydt, m * p.ldy + o, z);
+            if (TP_CHECK(p.err, m * p.ldy + o < p.y_extent)) store_out(p.Y, p.ydt, m * p.ldy + o, z);
           } else {
             int i = 0;
             while (i + 1 < p.tp && p.fo[i + 1] <= o) ++i;
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constan
               if (p.bias[i]) z += p.bias[i][n];
               if constexpr (ACT == TP_ACT_GELU_ERF) z = act_gelu_erf(z);
             }
-            store_out(p.Y, p.ydt, p.yoff[i] + m * p.ldy + n, z);
+            if (TP_CHECK(p.err, p.yoff[i] + m * p.ldy + n < p.y_extent))
+              store_out(p.Y, p.ydt, p.yoff[i] + m * p.ldy + n, z);
           }
         }
     }
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constan
 }
 
 template <int MT, int R, int U, int ACT, bool ROW>
-tp_status launch_fp8(const Fp8Params& gp, cudaStream_t stream) {
+tp_status prepare_fp8(const Fp8Params& gp, Launch* L) {
   auto kern = gemv_fp8_kernel<MT, R, U, ACT, ROW>;
   static int resident = 0;
   static std::once_flag once;
@@ -260,18 +262,22 @@ tp_status launch_fp8(const Fp8Params& gp, cudaStream_t stream) {
   });
   const int64_t n_tasks = (gp.n_out + R - 1) / R;
   const int64_t want = (n_tasks + kWarps - 1) / kWarps;
-  const int grid = (int)std::max<int64_t>(1, std::min(want, (int64_t)resident * sm_count()));
-  kern<<<grid, kThreads, 0, stream>>>(gp);
-  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  L->kernel = reinterpret_cast<const void*>(kern);
+  L->grid = dim3((unsigned)std::max<int64_t>(1, std::min(want, (int64_t)resident * sm_count())));
+  L->block = dim3(kThreads);
+  L->smem = 0;
+  L->cluster = 0;
+  L->set_params(gp);
+  return TP_OK;
 }
 
 template <int ACT, bool ROW>
-tp_status dispatch_fp8_mt(const Fp8Params& gp, cudaStream_t s) {
+tp_status dispatch_fp8_mt(const Fp8Params& gp, Launch* L) {
   constexpr bool SW = (ACT == TP_ACT_SWIGLU);
-  if (gp.M <= 1) return launch_fp8<1, SW ? 2 : 4, 2, ACT, ROW>(gp, s);
-  if (gp.M <= 2) return launch_fp8<2, SW ? 2 : 4, 2, ACT, ROW>(gp, s);
-  if (gp.M <= 4) return launch_fp8<4, SW ? 2 : 4, 1, ACT, ROW>(gp, s);
-  return launch_fp8<8, SW ? 2 : 4, 1, ACT, ROW>(gp, s);
+  if (gp.M <= 1) return prepare_fp8<1, SW ? 2 : 4, 2, ACT, ROW>(gp, L);
+  if (gp.M <= 2) return prepare_fp8<2, SW ? 2 : 4, 2, ACT, ROW>(gp, L);
+  if (gp.M <= 4) return prepare_fp8<4, SW ? 2 : 4, 1, ACT, ROW>(gp, L);
+  return prepare_fp8<8, SW ? 2 : 4, 1, ACT, ROW>(gp, L);
 }
 
 }  // namespace
@@ -285,7 +291,7 @@ tp_status launch_quantize_fp8(const void* W, int64_t rows, int64_t cols, void* Q
   return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
-tp_status launch_gemv_fp8(const LinearProblem& p, cudaStream_t stream) {
+tp_status prepare_gemv_fp8(const LinearProblem& p, Launch* L) {
   Fp8Params gp{};
   gp.tp = p.tp;
   gp.act = p.act;
@@ -302,16 +308,18 @@ tp_status launch_gemv_fp8(const LinearProblem& p, cudaStream_t stream) {
   gp.Y = p.Y;
   for (int i = 0; i < p.tp; ++i) gp.wrows[i] = p.row ? p.w_rows : p.wr[i];
   gp.err = device_error_word();
+  if (!gp.err) return TP_ERR_CUDA;
+  gp.y_extent = output_extent(p);
   for (int i = 0; i < TP_MAX_TP; ++i) {
     gp.W[i] = static_cast<const uint8_t*>(p.W[i]);
     gp.S[i] = p.wscale[i];
     gp.bias[i] = p.bias[i];
   }
-  if (p.row) return dispatch_fp8_mt<TP_ACT_NONE, true>(gp, stream);
+  if (p.row) return dispatch_fp8_mt<TP_ACT_NONE, true>(gp, L);
   switch (p.act) {
-    case TP_ACT_NONE: return dispatch_fp8_mt<TP_ACT_NONE, false>(gp, stream);
-    case TP_ACT_GELU_ERF: return dispatch_fp8_mt<TP_ACT_GELU_ERF, false>(gp, stream);
-    case TP_ACT_SWIGLU: return dispatch_fp8_mt<TP_ACT_SWIGLU, false>(gp, stream);
+    case TP_ACT_NONE: return dispatch_fp8_mt<TP_ACT_NONE, false>(gp, L);
+    case TP_ACT_GELU_ERF: return dispatch_fp8_mt<TP_ACT_GELU_ERF, false>(gp, L);
+    case TP_ACT_SWIGLU: return dispatch_fp8_mt<TP_ACT_SWIGLU, false>(gp, L);
   }
   return TP_ERR_BAD_SHAPE;
 }

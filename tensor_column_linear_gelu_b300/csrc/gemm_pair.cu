@@ -79,6 +79,7 @@ struct PairParams {
   CUtensorMap tmB[TP_MAX_TP];  // W_i.  Box {64, 128}.
   const float* bias[TP_MAX_TP];
   void* Y;
+  int64_t y_extent;  // elements of Y this call may write (checked builds)
   unsigned int* err;
   int64_t ldy, y_shard_stride;
   int64_t M, ns, n_out;
@@ -287,7 +288,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
           for (int j = 0; j < 32; ++j) g[j] = act_silu(g[j]) * u[j];
           const int64_t n = out0 + ch * 32;
           const int valid = valid_count(p.ns, n);
-          if (row_ok && valid > 0) store_row32(p.Y, p.ydt, base, n, valid, g);
+          if (row_ok && valid > 0 && TP_CHECK(p.err, base + n + valid <= p.y_extent))
+            store_row32(p.Y, p.ydt, base, n, valid, g);
         }
       } else {
         const int64_t limit = p.row ? p.n_out : p.ns;
@@ -308,7 +310,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = act_gelu_erf(v[j]);
           }
-          if (row_ok && valid > 0) store_row32(p.Y, p.ydt, base, n, valid, v);
+          if (row_ok && valid > 0 && TP_CHECK(p.err, base + n + valid <= p.y_extent))
+            store_row32(p.Y, p.ydt, base, n, valid, v);
         }
       }
       tc_fence_before();
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
 
 }  // namespace
 
-tp_status launch_gemm_pair(const LinearProblem& p, cudaStream_t stream) {
+tp_status prepare_gemm_pair(const LinearProblem& p, Launch* L) {
   PairParams gp{};
   gp.err = device_error_word();
   if (!gp.err) return TP_ERR_CUDA;
@@ -356,6 +359,7 @@ tp_status launch_gemm_pair(const LinearProblem& p, cudaStream_t stream) {
   for (int i = 0; i < TP_MAX_TP; ++i) gp.bias[i] = p.bias[i];
   gp.Y = p.Y;
   gp.ldy = p.ldy;
+  gp.y_extent = output_extent(p);
   gp.y_shard_stride = p.y_shard_stride;
   gp.M = p.M;
   gp.ns = p.ns;
@@ -387,20 +391,13 @@ tp_status launch_gemm_pair(const LinearProblem& p, cudaStream_t stream) {
   });
   if (attr_err != cudaSuccess) return TP_ERR_CUDA;
   const int pairs = (int)std::min<int64_t>(tiles, sm_count() / 2);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * std::max(pairs, 1)));
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = (size_t)SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gemm_pair_kernel, gp) != cudaSuccess) return TP_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  L->kernel = reinterpret_cast<const void*>(gemm_pair_kernel);
+  L->grid = dim3((unsigned)(2 * std::max(pairs, 1)));
+  L->block = dim3(THREADS);
+  L->smem = (size_t)SMEM_BYTES;
+  L->cluster = 2;
+  L->set_params(gp);
+  return TP_OK;
 }
 
 }  // namespace tpla

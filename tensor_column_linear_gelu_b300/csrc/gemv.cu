@@ -47,6 +47,7 @@ struct GemvParams {
   void* Y;
   int64_t wrows[TP_MAX_TP];   // rows of each weight shard buffer (checked builds)
   unsigned int* err;          // device error word (checked builds)
+  int64_t y_extent;           // elements of Y this call may write (checked builds)
 };
 
 template <typename T>
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
           float z = acc[mm][r];
           if constexpr (ROW) {
             if (p.bias[0]) z += p.bias[0][o];
-            store_out(p.Y, p.ydt, m * p.ldy + o, z);
+            if (TP_CHECK(p.err, m * p.ldy + o < p.y_extent)) store_out(p.Y, p.ydt, m * p.ldy + o, z);
           } else {
             int i = 0;
             while (i + 1 < p.tp && p.fo[i + 1] <= o) ++i;
@@ -198,16 +199,17 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const __grid_constant__ 
               if (p.bias[i]) z += p.bias[i][n];
               if constexpr (ACT == TP_ACT_GELU_ERF) z = act_gelu_erf(z);
             }
-            store_out(p.Y, p.ydt, p.yoff[i] + m * p.ldy + n, z);
+            if (TP_CHECK(p.err, p.yoff[i] + m * p.ldy + n < p.y_extent))
+              store_out(p.Y, p.ydt, p.yoff[i] + m * p.ldy + n, z);
           }
         }
     }
   }
 }
 
-// Launch one instantiation with a grid capped at (resident blocks x SMs).
+// Prepare one instantiation with a grid capped at (resident blocks x SMs).
 template <typename T, int MT, int R, int U, int ACT, bool ROW>
-tp_status launch_one(const GemvParams& gp, cudaStream_t stream) {
+tp_status prepare_one(const GemvParams& gp, Launch* L) {
   auto kern = gemv_kernel<T, MT, R, U, ACT, ROW>;
   static int resident = 0;  // blocks per SM for this instantiation
   static std::once_flag once;
@@ -220,36 +222,40 @@ tp_status launch_one(const GemvParams& gp, cudaStream_t stream) {
   const int64_t n_tasks = (gp.n_out + R - 1) / R;
   const int64_t want = (n_tasks + kWarps - 1) / kWarps;
   const int64_t cap = (int64_t)resident * sm_count();
-  const int grid = (int)std::max<int64_t>(1, std::min(want, cap));
-  kern<<<grid, kThreads, 0, stream>>>(gp);
-  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  L->kernel = reinterpret_cast<const void*>(kern);
+  L->grid = dim3((unsigned)std::max<int64_t>(1, std::min(want, cap)));
+  L->block = dim3(kThreads);
+  L->smem = 0;
+  L->cluster = 0;
+  L->set_params(gp);
+  return TP_OK;
 }
 
 // Tokens per pass (MT) and outputs per warp (R): the accumulator array
 // acc[MT][R or 2R] stays within ~32 registers.
 template <typename T, int ACT, bool ROW>
-tp_status dispatch_mt(const GemvParams& gp, cudaStream_t s) {
+tp_status dispatch_mt(const GemvParams& gp, Launch* L) {
   constexpr bool SW = (ACT == TP_ACT_SWIGLU);
-  if (gp.M <= 1) return launch_one<T, 1, SW ? 2 : 4, 4, ACT, ROW>(gp, s);
-  if (gp.M <= 2) return launch_one<T, 2, SW ? 2 : 4, 4, ACT, ROW>(gp, s);
-  if (gp.M <= 4) return launch_one<T, 4, SW ? 2 : 4, 2, ACT, ROW>(gp, s);
-  return launch_one<T, 8, SW ? 2 : 4, 2, ACT, ROW>(gp, s);
+  if (gp.M <= 1) return prepare_one<T, 1, SW ? 2 : 4, 4, ACT, ROW>(gp, L);
+  if (gp.M <= 2) return prepare_one<T, 2, SW ? 2 : 4, 4, ACT, ROW>(gp, L);
+  if (gp.M <= 4) return prepare_one<T, 4, SW ? 2 : 4, 2, ACT, ROW>(gp, L);
+  return prepare_one<T, 8, SW ? 2 : 4, 2, ACT, ROW>(gp, L);
 }
 
 template <typename T>
-tp_status dispatch_act(const LinearProblem& p, const GemvParams& gp, cudaStream_t s) {
-  if (p.row) return dispatch_mt<T, TP_ACT_NONE, true>(gp, s);
+tp_status dispatch_act(const LinearProblem& p, const GemvParams& gp, Launch* L) {
+  if (p.row) return dispatch_mt<T, TP_ACT_NONE, true>(gp, L);
   switch (p.act) {
-    case TP_ACT_NONE: return dispatch_mt<T, TP_ACT_NONE, false>(gp, s);
-    case TP_ACT_GELU_ERF: return dispatch_mt<T, TP_ACT_GELU_ERF, false>(gp, s);
-    case TP_ACT_SWIGLU: return dispatch_mt<T, TP_ACT_SWIGLU, false>(gp, s);
+    case TP_ACT_NONE: return dispatch_mt<T, TP_ACT_NONE, false>(gp, L);
+    case TP_ACT_GELU_ERF: return dispatch_mt<T, TP_ACT_GELU_ERF, false>(gp, L);
+    case TP_ACT_SWIGLU: return dispatch_mt<T, TP_ACT_SWIGLU, false>(gp, L);
   }
   return TP_ERR_BAD_SHAPE;
 }
 
 }  // namespace
 
-tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream) {
+tp_status prepare_gemv(const LinearProblem& p, Launch* L) {
   GemvParams gp{};
   gp.tp = p.tp;
   gp.act = p.act;
@@ -271,8 +277,10 @@ tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream) {
   }
   for (int i = 0; i < p.tp; ++i) gp.wrows[i] = p.row ? p.w_rows : p.wr[i];
   gp.err = device_error_word();
-  if (p.xdt == TP_F32) return dispatch_act<float>(p, gp, stream);
-  return dispatch_act<__nv_bfloat16>(p, gp, stream);
+  if (!gp.err) return TP_ERR_CUDA;
+  gp.y_extent = output_extent(p);
+  if (p.xdt == TP_F32) return dispatch_act<float>(p, gp, L);
+  return dispatch_act<__nv_bfloat16>(p, gp, L);
 }
 
 }  // namespace tpla

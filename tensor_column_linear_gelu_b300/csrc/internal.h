@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -55,12 +56,50 @@ struct LinearProblem {
   const float* wscale[TP_MAX_TP] = {};
 };
 
+// Number of elements of Y a problem may write: one past its last output
+// element.  Checked builds bound every output store by it.
+inline int64_t output_extent(const LinearProblem& p) {
+  if (p.M <= 0) return 0;
+  if (p.row) return (p.M - 1) * p.ldy + p.n_out;
+  int64_t e = 0;
+  for (int i = 0; i < p.tp; ++i) {
+    const int64_t ei = p.yoff[i] + (p.M - 1) * p.ldy + (p.fo[i + 1] - p.fo[i]);
+    if (ei > e) e = ei;
+  }
+  return e;
+}
+
+// A kernel launch prepared in full on the host: the kernel, its parameter
+// block (tensor maps already encoded), grid, block, dynamic shared memory and
+// cluster size.  Preparing does every host step that can fail except the
+// launch itself, so a call that issues several launches prepares all of them
+// before the first one starts: an error then leaves every output untouched.
+// kernel == nullptr means there is nothing to launch (no tokens).
+constexpr size_t kLaunchParamBytes = 8192;
+struct Launch {
+  const void* kernel = nullptr;
+  dim3 grid{1, 1, 1};
+  dim3 block{1, 1, 1};
+  size_t smem = 0;
+  unsigned cluster = 0;  // CTAs per cluster along x; 0: launched without clusters
+  alignas(64) unsigned char params[kLaunchParamBytes];
+  template <class P>
+  void set_params(const P& p) {
+    static_assert(sizeof(P) <= kLaunchParamBytes, "kernel parameter block too large");
+    std::memcpy(params, &p, sizeof(P));
+  }
+};
+// Launch a prepared kernel on `stream` (nothing when L.kernel is null).
+tp_status fire(const Launch& L, cudaStream_t stream);
+
+// Each prepare_* fills a Launch for one validated problem.
+
 // Weight-streaming GEMV on CUDA cores (few tokens; also the fp32 path).
-tp_status launch_gemv(const LinearProblem& p, cudaStream_t stream);
+tp_status prepare_gemv(const LinearProblem& p, Launch* L);
 
 // tcgen05 / TMEM tensor-core GEMM fed by TMA on CTA pairs (bf16; many
 // tokens; 256 x 256 tiles).
-tp_status launch_gemm_pair(const LinearProblem& p, cudaStream_t stream);
+tp_status prepare_gemm_pair(const LinearProblem& p, Launch* L);
 
 // tcgen05 decode kernel with the weights as the MMA's N operand (a handful
 // of tokens, up to kSkinnyMaxTokens; bf16 weights, or e4m3 weights widened
@@ -69,7 +108,7 @@ constexpr int64_t kSkinnyMaxTokens = 128;
 constexpr int kSkinnyMaxCluster = 8;  // CTAs per cluster on its row side
 // bf16 calls with at most this many tokens go to the GEMV.
 constexpr int64_t kGemvMaxTokens = 2;
-tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream);
+tp_status prepare_skinny(const LinearProblem& p, Launch* L);
 
 // 2-D bf16 tensor map for TMA: `rows` rows of `inner` elements, row pitch
 // ld_bytes, boxes of 64 elements (one 128-byte swizzle span) x box_rows rows,
@@ -88,14 +127,14 @@ bool make_tma_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_
 // per-row quantizer; the weight-streaming FP8 GEMV (M <= kGemvMaxTokens, and
 // row-parallel calls whose tp exceeds the largest cluster); the FP8 decode
 // kernel with the widened weights in tensor memory (M <= kFp8TmemMaxTokens);
-// above that the shared-memory decode kernel in its FP8 mode (launch_skinny
+// above that the shared-memory decode kernel in its FP8 mode (prepare_skinny
 // with p.fp8).
 constexpr int64_t kFp8MaxTokens = kSkinnyMaxTokens;
 constexpr int64_t kFp8TmemMaxTokens = 64;
-tp_status launch_decode_fp8(const LinearProblem& p, cudaStream_t stream);
+tp_status prepare_decode_fp8(const LinearProblem& p, Launch* L);
 tp_status launch_quantize_fp8(const void* W, int64_t rows, int64_t cols, void* Q, float* S,
                               cudaStream_t stream);
-tp_status launch_gemv_fp8(const LinearProblem& p, cudaStream_t stream);
+tp_status prepare_gemv_fp8(const LinearProblem& p, Launch* L);
 
 // Ring-ordered sum of per-shard partials ([tp][M][N], wire dtype) + bias.
 tp_status launch_ring_reduce(int tp, int64_t M, int64_t N, const void* parts, int wire_dt,

@@ -150,6 +150,7 @@ struct SkinnyParams {
   void* Y;
   unsigned int* err;
   int64_t ldy;
+  int64_t y_extent;              // elements of Y this call may write (checked builds)
   int64_t fo[TP_MAX_TP + 1];     // column: shard i owns features [fo[i], fo[i+1])
   int64_t yoff[TP_MAX_TP];       // column: element offset of shard i's outputs in Y
   int64_t M, feat_total;         // feat_total: column fo[tp]; row n_out
@@ -539,6 +540,7 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
                   for (int j = 0; j < CH; ++j) v[j] = act_gelu_erf(v[j]);
                 }
               }
+              if (!TP_CHECK(p.err, base + pc.loc + j0 + valid <= p.y_extent)) continue;
               if constexpr (CH == 16)
                 store_row16(p.Y, p.ydt, base, pc.loc + j0, valid, v);
               else
@@ -662,7 +664,8 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
         float sum = 0.0f;
         for (int r = 0; r < p.cs; ++r) sum += dsmem_ld_f32(dsmem_addr(red_s + off, (uint32_t)r));
         if (bias) sum += __ldg(bias + loc + j);
-        store_out(p.Y, p.ydt, tok * p.ldy + loc + j, sum);
+        if (TP_CHECK(p.err, tok * p.ldy + loc + j < p.y_extent))
+          store_out(p.Y, p.ydt, tok * p.ldy + loc + j, sum);
       }
     }
     cluster_sync_all();  // no CTA leaves while a peer still reads its buffer
@@ -677,7 +680,7 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
 #undef SK_FOR_EACH_TILE
 
 template <bool F8>
-tp_status launch_skinny_mode(const LinearProblem& p, cudaStream_t stream) {
+tp_status prepare_skinny_mode(const LinearProblem& p, Launch* L) {
   if (p.xdt != TP_BF16 || p.M < 1 || p.M > kSkinnyMaxTokens) return TP_ERR_UNSUPPORTED;
   if (F8 && p.row && p.tp > SK_MAX_CLUSTER) return TP_ERR_UNSUPPORTED;
   SkinnyParams sp{};
@@ -716,6 +719,7 @@ tp_status launch_skinny_mode(const LinearProblem& p, cudaStream_t stream) {
   }
   sp.Y = p.Y;
   sp.ldy = p.ldy;
+  sp.y_extent = output_extent(p);
   for (int i = 0; i <= p.tp; ++i) sp.fo[i] = p.fo[i];
   for (int i = 0; i < p.tp; ++i) sp.yoff[i] = p.yoff[i];
   sp.M = p.M;
@@ -797,26 +801,19 @@ tp_status launch_skinny_mode(const LinearProblem& p, cudaStream_t stream) {
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_MAX);
   });
   if (attr_err != cudaSuccess) return TP_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(F8 ? SK_THREADS_F8 : SK_THREADS);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)sp.cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, skinny_kernel<F8>, sp) != cudaSuccess) return TP_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  L->kernel = reinterpret_cast<const void*>(skinny_kernel<F8>);
+  L->grid = dim3((unsigned)grid);
+  L->block = dim3(F8 ? SK_THREADS_F8 : SK_THREADS);
+  L->smem = (size_t)smem;
+  L->cluster = (unsigned)sp.cs;
+  L->set_params(sp);
+  return TP_OK;
 }
 
 }  // namespace
 
-tp_status launch_skinny(const LinearProblem& p, cudaStream_t stream) {
-  return p.fp8 ? launch_skinny_mode<true>(p, stream) : launch_skinny_mode<false>(p, stream);
+tp_status prepare_skinny(const LinearProblem& p, Launch* L) {
+  return p.fp8 ? prepare_skinny_mode<true>(p, L) : prepare_skinny_mode<false>(p, L);
 }
 
 }  // namespace tpla
