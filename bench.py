@@ -432,36 +432,51 @@ class Path:
                 "uneven": self.w["tp"]}.get(self.w["kind"], 2)
 
 
-def run_ours(args, w, rank, local_rank, world):
+# Datasheet figures of one B300, for the second denominator of every
+# fraction: HBM3e bandwidth, and the dense (no 2:4 sparsity) bf16 tensor peak.
+DATASHEET = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0,
+             "source": "B300 datasheet: HBM3e 8 TB/s; bf16 dense 2.25 PFLOP/s"}
+
+# Decode-shaped workloads timed in the default run next to the headline one.
+DECODE_EXTRAS = ("swiglu_ffn_decode_tp4_b1", "swiglu_ffn_decode_tp4_b8",
+                 "swiglu_ffn_decode_tp4_b32", "swiglu_ffn_decode_tp4_b64",
+                 "swiglu_ffn_decode_tp4_b1_fp8", "swiglu_ffn_decode_tp4_b8_fp8")
+
+
+def measure(args, name, w, dev, world, steps, warmup):
+    """Time `steps` steps of workload `w` on device `dev` (after `warmup`
+    untimed ones), with CUDA events on the launching stream.  Returns the
+    timing, the roofline of the dominant launch and of the whole step, and the
+    SM clocks sampled during the timed region.  `path` is returned too, for the
+    end-to-end leg."""
     import torch
     from tensor_column_linear_gelu_b300 import tpla
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
     peaks = load_peaks()
     path = Path(w, dev)
     s = torch.cuda.Stream(device=dev)
     parts = path.parts()
     work = kernel_work(w)
     step_bytes = sum(b for _, b in work.values())
+    step_flops = sum(f for f, _ in work.values())
     flush = None
     if step_bytes < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     with torch.cuda.stream(s):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             for _, fn in parts:
                 fn(s)
     s.synchronize()
     st = tpla.tp_device_status(s)
     if st != tpla.TP_OK:
-        raise RuntimeError(f"device status after warm-up: {tpla.status_string(st)}")
+        raise RuntimeError(f"{name}: device status after warm-up: {tpla.status_string(st)}")
 
-    K = args.steps
+    K = steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(dev.index)
     with clocks:
         with torch.cuda.stream(s):
             for k in range(K):
@@ -477,10 +492,10 @@ def run_ours(args, w, rank, local_rank, world):
     torch.cuda.synchronize()
     st = tpla.tp_device_status(s)
     if st != tpla.TP_OK:
-        raise RuntimeError(f"device status after timed region: {tpla.status_string(st)}")
+        raise RuntimeError(f"{name}: device status after timed region: {tpla.status_string(st)}")
 
-    per_part = {name: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)]
-                for j, (name, _) in enumerate(parts)}
+    per_part = {pn: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)]
+                for j, (pn, _) in enumerate(parts)}
     step_ms = [ev[k][0].elapsed_time(ev[k][len(parts)]) for k in range(K)]
     # Steps run back to back: with no flush the span first->last event is the
     # timed region on the device; with a flush the flushes are excluded.
@@ -512,66 +527,134 @@ def run_ours(args, w, rank, local_rank, world):
         launches_in_dom = 2
     bound = "tensor" if flops / nbytes > ridge else "hbm"
     long_region = elapsed_ms > 1000.0
+    step_s = (elapsed_ms / K) / 1e3
     if bound == "tensor":
         peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
         achieved = flops / dur_s / 1e12
+        step_achieved = step_flops / step_s / 1e12
         unit = "TFLOP/s"
         peak_kind = ("sustained" if long_region else "burst") + " bf16, " + peaks["source"]
+        sheet = DATASHEET["bf16_tflops"]
     else:
         peak = peaks["hbm_gbs"]
         achieved = nbytes / dur_s / 1e9
+        step_achieved = step_bytes / step_s / 1e9
         unit = "GB/s"
         peak_kind = "hbm copy, " + peaks["source"]
-    tr = traffic_record(args.workload)
+        sheet = DATASHEET["hbm_gbs"]
+    tr = traffic_record(name)
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": tr.get("bytes_per_launch"),
                 "kernel": dom, "launches": launches_in_dom,
                 "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
-                "avg_ms": round(dur_s * 1e3, 4), "peak_kind": peak_kind}
+                "avg_ms": round(dur_s * 1e3, 4), "peak_kind": peak_kind,
+                "datasheet_peak": sheet, "frac_of_datasheet": round(achieved / sheet, 4),
+                "step": {"achieved": round(step_achieved, 2), "unit": unit,
+                         "frac": round(step_achieved / peak, 4),
+                         "frac_of_datasheet": round(step_achieved / sheet, 4),
+                         "algorithmic_flops": step_flops, "algorithmic_bytes": step_bytes}}
     if tr.get("bytes_per_launch") is not None:
         roofline["traffic_source"] = tr.get("source")
-
-    e2e = run_e2e(path, w, s, args)
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, budget_s=args.cpu_seconds)
-
     return dict(elapsed_max=elapsed_max, tokens_all=tokens_all, roofline=roofline,
                 per_part={n: round(sum(v) / len(v), 4) for n, v in per_part.items()},
-                clocks=clocks.summary(), e2e=e2e, cpu=cpu, flush=flush is not None,
-                launches=K * path.launches_per_step())
+                clocks=clocks.summary(), flush=flush is not None,
+                launches=K * path.launches_per_step(), path=path, stream=s)
+
+
+def run_ours(args, w, rank, local_rank, world):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    r = measure(args, args.workload, w, dev, world, args.steps, args.warmup)
+    r["e2e"] = run_e2e(r.pop("path"), w, r.pop("stream"), args)
+    torch.cuda.empty_cache()
+    r["cpu"] = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r["cpu"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    # the decode-shaped workloads, each with its own roofline (HBM-bound)
+    r["decode"] = None
+    if args.workload == DEFAULT_WORKLOAD and not args.no_decode:
+        r["decode"] = {}
+        for name in DECODE_EXTRAS:
+            wd = WORKLOADS[name]
+            d = measure(args, name, wd, dev, world, args.decode_steps, args.warmup)
+            d.pop("path")
+            d.pop("stream")
+            torch.cuda.empty_cache()
+            d["value"] = round(d["tokens_all"] / (d["elapsed_max"] / 1e3), 2)
+            d["ms_per_step"] = round(d["elapsed_max"] / args.decode_steps, 4)
+            d["steps"] = args.decode_steps
+            d["kernel_ms"] = d.pop("per_part")
+            d["unit"] = "tokens/s"
+            d["gpu_launches"] = d.pop("launches")
+            for k in ("elapsed_max", "tokens_all", "flush"):
+                d.pop(k)
+            r["decode"][name] = d
+    return r
 
 
 def run_e2e(path, w, s, args):
-    """Same metric through the public call, with the step's input copied in from
-    pinned host memory and the result read back to pinned host memory, every step."""
+    """Same metric through the public call, with each step's input copied in
+    from pinned host memory and its result read back to pinned host memory.
+
+    Copies run on their own streams so that step k+1's input copy and step
+    k-1's result copy overlap step k's kernels; inputs and outputs are
+    double-buffered, and events order each buffer's reuse.  The timed region
+    runs from before the first input copy to after the last result copy."""
     import torch
+    dev = path.X.device
     Xh = path.X.to("cpu").pin_memory()
-    Yh = torch.empty(path.Y.shape, dtype=path.Y.dtype).pin_memory()
-    Xd = torch.empty_like(path.X)
-    Yd = torch.empty_like(path.Y)
+    Yh = [torch.empty(path.Y.shape, dtype=path.Y.dtype).pin_memory() for _ in range(2)]
+    Xd = [torch.empty_like(path.X) for _ in range(2)]
+    Yd = [torch.empty_like(path.Y) for _ in range(2)]
+    cin = torch.cuda.Stream(device=dev)
+    cout = torch.cuda.Stream(device=dev)
     K = args.steps
-    with torch.cuda.stream(s):
-        for _ in range(max(1, args.warmup)):
-            Xd.copy_(Xh, non_blocking=True)
-            path.step_public(s, Xd, Yd)
-            Yh.copy_(Yd, non_blocking=True)
+
+    def run(n_steps):
+        x_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [None, None]     # step k's kernels finished with Xd/Yd[k % 2]
+        out_done = [None, None]  # result copy of Yd[k % 2] finished
+        for k in range(n_steps):
+            b = k % 2
+            if done[b] is not None:
+                cin.wait_event(done[b])
+            with torch.cuda.stream(cin):
+                Xd[b].copy_(Xh, non_blocking=True)
+                x_ready[b].record(cin)
+            s.wait_event(x_ready[b])
+            if out_done[b] is not None:
+                s.wait_event(out_done[b])
+            with torch.cuda.stream(s):
+                path.step_public(s, Xd[b], Yd[b])
+                done[b] = torch.cuda.Event()
+                done[b].record(s)
+            cout.wait_event(done[b])
+            with torch.cuda.stream(cout):
+                Yh[b].copy_(Yd[b], non_blocking=True)
+                out_done[b] = torch.cuda.Event()
+                out_done[b].record(cout)
+        for e in out_done:
+            if e is not None:
+                s.wait_event(e)
+
+    run(max(1, args.warmup))
     s.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
-        for _ in range(K):
-            Xd.copy_(Xh, non_blocking=True)
-            path.step_public(s, Xd, Yd)
-            Yh.copy_(Yd, non_blocking=True)
-        e1.record(s)
+    e0.record(s)
+    cin.wait_event(e0)
+    run(K)
+    e1.record(s)
     s.synchronize()
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     return {"value": round(w["M"] * K / (ms / 1e3), 2), "unit": "tokens/s",
             "h2d_bytes_per_step": Xh.numel() * Xh.element_size(),
-            "d2h_bytes_per_step": Yh.numel() * Yh.element_size(),
-            "ms_per_step": round(ms / K, 4)}
+            "d2h_bytes_per_step": Yh[0].numel() * Yh[0].element_size(),
+            "ms_per_step": round(ms / K, 4),
+            "overlap": "input copy of step k+1 and result copy of step k-1 on their own "
+                       "streams, double-buffered, overlapping step k"}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -650,23 +733,23 @@ def oracle_step(orc, w, a):
 
 
 def cpu_baseline(w, budget_s=15.0):
-    """The oracle, as it stands, on a bounded sample of the workload's rows."""
+    """The oracle, as it stands, on a bounded sample of the workload's rows: the
+    sample grows until one timed run takes at least budget_s / 2 (about
+    budget_s of CPU work in all), or covers every row."""
     import oracle
     from tensor_column_linear_gelu_b300 import inputs
     orc = oracle.default()
-    rows = inputs.sample_rows(w["M"], 1, 20_000)
-    a = oracle_inputs(w, rows)
-    t0 = time.perf_counter()
-    oracle_step(orc, w, a)
-    t1 = time.perf_counter() - t0
-    n = int(max(1, min(w["M"], math.floor(budget_s / max(t1, 1e-3)))))
-    if n > 1:
+    n = 1
+    while True:
         rows = inputs.sample_rows(w["M"], n, 20_000)
         a = oracle_inputs(w, rows)
         t0 = time.perf_counter()
         oracle_step(orc, w, a)
         t1 = time.perf_counter() - t0
-    n = len(rows)
+        n = len(rows)
+        if t1 >= budget_s / 2 or n >= w["M"]:
+            break
+        n = int(min(w["M"], max(2 * n, math.ceil(n * 0.6 * budget_s / max(t1, 1e-3)))))
     return {"value": round(n / t1, 4), "unit": "tokens/s", "cores": orc.num_threads(),
             "kind": "oracle",
             "sample": f"{n} of {w['M']} rows of the same workload (fp64 C oracle, OpenMP), "
@@ -719,6 +802,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-shaped workloads timed next to the default one")
+    ap.add_argument("--decode-steps", type=int, default=50)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -756,6 +842,8 @@ def main():
             "gpu_launches": r["launches"], "clocks": r["clocks"],
             "kernel_ms": r["per_part"],
         }
+        if r.get("decode"):
+            line["decode"] = r["decode"]
         n_ar = {"ffn": 1, "attn": 1, "layer": 2, "row_ring": 1}.get(w["kind"], 0)
         if n_ar:
             msg = 2.0 * w["M"] * w["d"]  # one bf16 [M, d_model] message per all-reduce

@@ -45,3 +45,17 @@ def test_fp8_work_model_halves_weight_bytes():
     assert f8["column"][0] == bf["column"][0] and f8["row"][0] == bf["row"][0]
     assert f8["column"][1] == bf["column"][1] - 2 * dff * d + 4 * 2 * dff
     assert f8["row"][1] == bf["row"][1] - dff * d + 4 * tp * d
+
+
+def test_decode_extras_and_datasheet_denominators():
+    """The default run also times the decode-shaped workloads; every fraction is
+    reported against the measured peaks and against the datasheet figures."""
+    assert set(bench.DECODE_EXTRAS) <= set(bench.WORKLOADS)
+    for name in bench.DECODE_EXTRAS:
+        w = bench.WORKLOADS[name]
+        assert w["kind"] == "ffn" and w["M"] <= 64
+        # decode is HBM-bound: its intensity is far below the ridge point
+        flops = sum(f for f, _ in bench.kernel_work(w).values())
+        nbytes = sum(b for _, b in bench.kernel_work(w).values())
+        assert flops / nbytes < 100
+    assert bench.DATASHEET["hbm_gbs"] == 8000.0 and bench.DATASHEET["bf16_tflops"] == 2250.0
