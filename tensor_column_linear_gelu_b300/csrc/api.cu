@@ -19,15 +19,22 @@ tp_status fire(const Launch& L, cudaStream_t stream) {
   cfg.blockDim = L.block;
   cfg.dynamicSmemBytes = L.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
   if (L.cluster > 0) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = L.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = L.cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
+  if (L.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   void* args[1] = {const_cast<unsigned char*>(L.params)};
   if (cudaLaunchKernelExC(&cfg, L.kernel, args) != cudaSuccess) return TP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
@@ -97,6 +104,7 @@ tp_status check_bias_array(const float* const* b, int tp) {
 //   bf16, kGemvMaxTokens < M <= kSkinnyMaxTokens  tcgen05 decode kernel
 //   bf16, M > kSkinnyMaxTokens                    tcgen05 prefill GEMM
 //   FP8 weights, M <= kGemvMaxTokens              FP8 weight-streaming GEMV
+//   FP8 weights, M <= kF8MmaMaxTokens             tcgen05 e4m3 x e4m3 decode kernel
 //   FP8 weights, M <= kFp8TmemMaxTokens           tcgen05 FP8 decode kernel, weights in TMEM
 //   FP8 weights, larger M                         tcgen05 decode kernel, FP8 mode
 // (FP8 row-parallel calls with tp above the decode kernels' largest cluster
@@ -107,6 +115,7 @@ tp_status prepare(const LinearProblem& p, Launch* L) {
   if (p.fp8) {
     if (p.M <= kGemvMaxTokens || (p.row && p.tp > kSkinnyMaxCluster))
       return prepare_gemv_fp8(p, L);
+    if (p.M <= kF8MmaMaxTokens) return prepare_f8mma(p, L);
     if (p.M <= kFp8TmemMaxTokens) return prepare_decode_fp8(p, L);
     return prepare_skinny(p, L);
   }

@@ -173,15 +173,20 @@ __device__ __forceinline__ Tile row_tile(const P& p, int rank) {
 }
 
 // Loop over this CTA's tiles: the column side walks its feature range, the
-// row side has one tile.
+// row side has one tile.  Inside the body, tile_is_last tells whether tl is
+// the CTA's last tile.
 #define SK_FOR_EACH_TILE(tl, ...)                                     \
   do {                                                                \
     if (p.row) {                                                      \
       const Tile tl = row_tile(p, rank);                              \
+      const bool tile_is_last = true;                                 \
+      (void)tile_is_last;                                             \
       __VA_ARGS__                                                     \
     } else {                                                          \
       for (int64_t f_ = f0; f_ < f1;) {                               \
         const Tile tl = column_tile(p, f_, f1);                       \
+        const bool tile_is_last = f_ >= f1;                           \
+        (void)tile_is_last;                                           \
         __VA_ARGS__                                                   \
       }                                                               \
     }                                                                 \

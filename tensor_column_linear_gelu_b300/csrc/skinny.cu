@@ -203,6 +203,10 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
   const int rank = p.row ? (int)cluster_ctarank() : 0;
   // row side, FP8 mode: the shard this CTA's k-range lies in
   const int rshard = p.row ? (int)((int64_t)rank * p.tp / p.cs) : 0;
+  // The next kernel may start its prologue now.  The producer waits for the
+  // kernels before this one before its first load (every stage carries X);
+  // everything that writes Y comes after its loads.
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < XS; ++s) {
@@ -256,6 +260,7 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
     int rs = 0;         // FP8: raw ring
     uint32_t rphase = 0;
     bool ok = true;
+    pdl_wait();  // X may be the output of the kernel before this one
     // X is re-read by every SM; the weights are streamed once.
     const uint64_t pol_x = l2_policy_evict_last();
     const uint64_t pol_w = l2_policy_evict_first();
@@ -806,6 +811,7 @@ tp_status prepare_skinny_mode(const LinearProblem& p, Launch* L) {
   L->block = dim3(F8 ? SK_THREADS_F8 : SK_THREADS);
   L->smem = (size_t)smem;
   L->cluster = (unsigned)sp.cs;
+  L->pdl = true;
   L->set_params(sp);
   return TP_OK;
 }

@@ -70,6 +70,36 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Instruction descriptor, kind::f8f6f4: D fp32, A and B e4m3 (format code 0),
+// both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.  One MMA
+// consumes K = 32 (32 bytes of each operand row).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (when it was launched with programmatic stream serialization)
+// start its prologue while this one runs; wait blocks until every preceding
+// kernel of the stream has completed and its memory writes are visible.  A
+// kernel calls wait before it touches memory that an earlier kernel may
+// write or read (its activations and its outputs); weights are written only
+// by set-up kernels, which never signal early, so they may be read before.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -108,6 +138,34 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive fp32 columns at each of two TMEM addresses of this thread's
+// lane (a SwiGLU output's gate and up accumulators), with one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32],
+                                            float (&b)[32]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[32 + i]);
+  }
 }
 
 // 16 consecutive fp32 columns at each of two TMEM addresses of this thread's
@@ -195,6 +253,34 @@ __device__ __forceinline__ void store_row32(void* Y, int ydt, int64_t base, int6
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
+        if (j < valid) p[j] = __float2bfloat16_rn(v[j]);
+    }
+  }
+}
+
+// 4 consecutive outputs v[0..3] of one row at columns n0.. (n0 + 3), of which
+// the first `valid` exist.  One vector store when the address allows.
+__device__ __forceinline__ void store_row4(void* Y, int ydt, int64_t base, int64_t n0, int valid,
+                                           const float (&v)[4]) {
+  if (ydt == TP_F32) {
+    float* p = reinterpret_cast<float*>(Y) + base + n0;
+    if (valid == 4 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+      *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < valid) p[j] = v[j];
+    }
+  } else {
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(Y) + base + n0;
+    if (valid == 4 && (reinterpret_cast<uintptr_t>(p) & 7u) == 0) {
+      uint2 q;
+      q.x = pack_bf16x2(v[0], v[1]);
+      q.y = pack_bf16x2(v[2], v[3]);
+      *reinterpret_cast<uint2*>(p) = q;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
         if (j < valid) p[j] = __float2bfloat16_rn(v[j]);
     }
   }
