@@ -10,6 +10,18 @@
 
 namespace tpla {
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (when it was launched with programmatic stream serialization)
+// start its prologue while this one runs; wait blocks until every preceding
+// kernel of the stream has completed and its memory writes are visible.  A
+// kernel calls wait before it touches memory that an earlier kernel may
+// write or read (its activations and its outputs); weights are written only
+// by set-up kernels, which never signal early, so they may be read before.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- activations
 // Applied in fp32 to the fp32 accumulator (plus bias) before the single
 // rounding to the output dtype.

@@ -150,6 +150,11 @@ __global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constan
   const int64_t warp_stride = (int64_t)gridDim.x * kWarps;
   const int64_t n_tasks = (p.n_out + R - 1) / R;
   const int64_t nvec = p.K / E;
+  // The next kernel may start now.  (This kernel is launched in plain
+  // stream order, so every kernel before it has completed; the wait returns
+  // at once and keeps the kernel correct under a programmatic launch too.)
+  pdl_launch_dependents();
+  pdl_wait();
 
   for (int64_t t = warp_global; t < n_tasks; t += warp_stride) {
     for (int64_t m0 = 0; m0 < p.M; m0 += MT) {
@@ -267,6 +272,10 @@ tp_status prepare_fp8(const Fp8Params& gp, Launch* L) {
   L->block = dim3(kThreads);
   L->smem = 0;
   L->cluster = 0;
+  // Launched in plain stream order (measured: a programmatic launch of the
+  // GEMV itself costs it 1-2 %); it still signals its dependents at entry,
+  // so a decode kernel after it starts early.
+  L->pdl = false;
   L->set_params(gp);
   return TP_OK;
 }

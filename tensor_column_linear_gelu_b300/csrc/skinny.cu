@@ -260,10 +260,29 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
     int rs = 0;         // FP8: raw ring
     uint32_t rphase = 0;
     bool ok = true;
-    pdl_wait();  // X may be the output of the kernel before this one
     // X is re-read by every SM; the weights are streamed once.
     const uint64_t pol_x = l2_policy_evict_last();
     const uint64_t pol_w = l2_policy_evict_first();
+    // X may be the output of the kernel before this one (programmatic
+    // dependent launch): bf16 mode issues the weight boxes of the first S
+    // stages at once and defers their X boxes (lane 0) until pdl_wait, so
+    // the weight stream starts while the previous kernel finishes.  FP8 mode
+    // waits first.
+    bool waited = F8;
+    if constexpr (F8) pdl_wait();
+    int nd = 0;  // deferred X boxes (lane 0): stage, k-block, shard
+    int d_stage[SK_MAX_STAGES], d_kk[SK_MAX_STAGES], d_sh[SK_MAX_STAGES];
+    auto flush_x = [&]() {
+      if (lane == 0) {
+        pdl_wait();
+        for (int i = 0; i < nd; ++i)
+          tma_load_2d_hint(smem_u32(sX + (size_t)d_stage[i] * p.x_stage_bytes), &p.tmX[d_sh[i]],
+                           d_kk[i] * SK_BK, 0, smem_u32(&full[d_stage[i]]), pol_x);
+      }
+      nd = 0;
+      waited = true;
+      __syncwarp();
+    };
     SK_FOR_EACH_TILE(tl, {
       if (ok) {
         int piece = 0, half = 0, r = 0, h = 0;
@@ -344,6 +363,7 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
           for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
             const int rsh = p.row ? kb / p.kb_per_shard : 0;  // row side: shard of this k-block
             const int kk = p.row ? kb - rsh * p.kb_per_shard : kb;
+            if (!waited && nd == S) flush_x();  // stage reuse needs the deferred X boxes
             bool got = true;
             if (lane == 0) got = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u);
             got = __shfl_sync(0xffffffffu, got, 0);
@@ -355,14 +375,21 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
             const uint32_t fb = smem_u32(&full[stage]);
             if (lane == 0) {
               mbar_arrive_expect_tx(fb, (uint32_t)p.x_stage_bytes + wbytes);
-              tma_load_2d_hint(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh],
-                               kk * SK_BK, 0, fb, pol_x);
+              if (waited) {
+                tma_load_2d_hint(smem_u32(sX + (size_t)stage * p.x_stage_bytes), &p.tmX[rsh],
+                                 kk * SK_BK, 0, fb, pol_x);
+              } else if (TP_CHECK(p.err, nd < SK_MAX_STAGES)) {
+                d_stage[nd] = stage;
+                d_kk[nd] = kk;
+                d_sh[nd] = rsh;
+              }
             } else if (mine) {
               const int sh = p.row ? rsh : wshard;
               const CUtensorMap* map = (h == 64) ? &p.tmW64[sh] : &p.tmW16[sh];
               tma_load_2d_hint(smem_u32(sW + (size_t)stage * p.w_stage_bytes) + woff, map,
                                kk * SK_BK, (int)wrow, fb, pol_w);
             }
+            if (!waited) ++nd;
             __syncwarp();
             if (++stage == S) {
               stage = 0;
@@ -372,6 +399,7 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
         }
       }
     });
+    if (!waited) flush_x();  // fewer stages than the ring holds
     // Every copy issued here is consumed by the MMA thread (same tile
     // sequence); the epilogue waits for the commit that follows the last one.
   } else if (warp == 1 && lane == 0) {

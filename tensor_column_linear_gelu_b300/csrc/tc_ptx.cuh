@@ -88,18 +88,6 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
-// Programmatic dependent launch.  launch_dependents lets the next kernel of
-// the stream (when it was launched with programmatic stream serialization)
-// start its prologue while this one runs; wait blocks until every preceding
-// kernel of the stream has completed and its memory writes are visible.  A
-// kernel calls wait before it touches memory that an earlier kernel may
-// write or read (its activations and its outputs); weights are written only
-// by set-up kernels, which never signal early, so they may be read before.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
