@@ -103,18 +103,17 @@ tp_status check_bias_array(const float* const* b, int tp) {
 //   fp32, or bf16 with M <= kGemvMaxTokens      weight-streaming GEMV (CUDA cores)
 //   bf16, kGemvMaxTokens < M <= kSkinnyMaxTokens  tcgen05 decode kernel
 //   bf16, M > kSkinnyMaxTokens                    tcgen05 prefill GEMM
-//   FP8 weights, M <= kGemvMaxTokens              FP8 weight-streaming GEMV
 //   FP8 weights, M <= kF8MmaMaxTokens             tcgen05 e4m3 x e4m3 decode kernel
 //   FP8 weights, M <= kFp8TmemMaxTokens           tcgen05 FP8 decode kernel, weights in TMEM
 //   FP8 weights, larger M                         tcgen05 decode kernel, FP8 mode
 // (FP8 row-parallel calls with tp above the decode kernels' largest cluster
-// also take the FP8 GEMV: their CTAs must each hold one shard's k-range.)
+// take the FP8 GEMV: the tensor-core kernels' CTAs must each hold one
+// shard's k-range.)
 tp_status prepare(const LinearProblem& p, Launch* L) {
   L->kernel = nullptr;
   if (p.M == 0) return TP_OK;
   if (p.fp8) {
-    if (p.M <= kGemvMaxTokens || (p.row && p.tp > kSkinnyMaxCluster))
-      return prepare_gemv_fp8(p, L);
+    if (p.row && p.tp > kSkinnyMaxCluster) return prepare_gemv_fp8(p, L);
     if (p.M <= kF8MmaMaxTokens) return prepare_f8mma(p, L);
     if (p.M <= kFp8TmemMaxTokens) return prepare_decode_fp8(p, L);
     return prepare_skinny(p, L);

@@ -127,16 +127,16 @@ bool make_tma_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_
                      uint64_t ld_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 
 // FP8 (e4m3) weights, bf16 activations, at most kFp8MaxTokens tokens: the
-// per-row quantizer; the weight-streaming FP8 GEMV (M <= kGemvMaxTokens, and
-// row-parallel calls whose tp exceeds the largest cluster); the e4m3 x e4m3
-// kernel (M <= kF8MmaMaxTokens); the FP8 decode kernel with the widened
+// per-row quantizer; the weight-streaming FP8 GEMV (row-parallel calls whose
+// tp exceeds the largest cluster); the e4m3 x e4m3 kernel (M <=
+// kF8MmaMaxTokens); the FP8 decode kernel with the widened
 // weights in tensor memory (M <= kFp8TmemMaxTokens);
 // above that the shared-memory decode kernel in its FP8 mode (prepare_skinny
 // with p.fp8).
 constexpr int64_t kFp8MaxTokens = kSkinnyMaxTokens;
 constexpr int64_t kFp8TmemMaxTokens = 64;
-// FP8 weights with at most this many tokens (and more than kGemvMaxTokens)
-// take the e4m3 x e4m3 tensor-core kernel: the codes stream straight into the
+// FP8 weights with at most this many tokens take the e4m3 x e4m3
+// tensor-core kernel: the codes stream straight into the
 // MMA's N operand and each token is split exactly into three e4m3 planes.
 constexpr int64_t kF8MmaMaxTokens = 32;
 tp_status prepare_f8mma(const LinearProblem& p, Launch* L);

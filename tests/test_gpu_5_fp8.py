@@ -1,4 +1,4 @@
-"""FP8 (e4m3) weights: the GPU quantizer and the FP8 weight-streaming GEMV.
+"""FP8 (e4m3) weights: the GPU quantizer and every FP8 compute kernel.
 
 * tp_quantize_fp8 decides integer codes, so it must match the oracle's
   quantizer bit for bit: the scale (fp32) and every e4m3 code, for ordinary
@@ -9,11 +9,13 @@
   weights itself; nothing it uses comes from the GPU.  Tolerance: the bf16
   one (5e-3 x RMS, fp32 output); the FFN's h (bf16) within half a bf16 ulp.
 * The FP8 column split is bit-identical to tp = 1, as the bf16 one is.
-* All three FP8 kernels are covered: the FP8 GEMV (one or two tokens), the
-  tensor-core kernel that widens the codes into tensor memory (3..64 tokens)
-  and the tensor-core decode kernel in its FP8 mode, which widens them into
-  shared memory (65..128 tokens): every one of the 254 finite e4m3 codes goes
-  through each kernel once and must come out as its exact value.
+* Every FP8 kernel is covered: the e4m3 x e4m3 tensor-core kernel (1..32
+  tokens: codes straight into the MMA, tokens split into three e4m3 planes),
+  the kernel that widens the codes into tensor memory (33..64 tokens), the
+  tensor-core decode kernel in its FP8 mode, which widens them into shared
+  memory (65..128 tokens), and the FP8 GEMV (row splits wider than a
+  cluster, tp > 8): every one of the 254 finite e4m3 codes goes through each
+  kernel once and must come out as its exact value.
 """
 import numpy as np
 import pytest
@@ -84,7 +86,7 @@ def test_fp8_column_parallel(orc, M, K, N, tp, act, bias):
     assert tpla.tp_device_status() == tpla.TP_OK
 
 
-# M, K, N, tp, bias  (tp = 16 row calls with M > 2 take the GEMV)
+# M, K, N, tp, bias  (tp = 16 row calls take the FP8 GEMV)
 ROW_CASES = [(1, 512, 64, 2, True), (3, 1536, 200, 3, False), (8, 4096, 256, 8, True),
              (16, 1024, 520, 4, True), (64, 2048, 1024, 2, False), (128, 512, 300, 1, True),
              (5, 4096, 96, 16, True), (40, 3072, 768, 6, False), (4, 544, 320, 2, True),
@@ -152,7 +154,7 @@ def e4m3_table() -> np.ndarray:
     return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
 
 
-@pytest.mark.parametrize("M", [1, 4, 100])
+@pytest.mark.parametrize("M", [1, 4, 40, 100])
 def test_every_e4m3_code_exact(orc, M):
     """W[n, k] = the value of code (n + k) mod 256 (NaN codes -> +-448), so every
     row holds 448, its scale is 1 and its codes are the table itself; token m is
@@ -176,3 +178,24 @@ def test_every_e4m3_code_exact(orc, M):
     assert np.array_equal(y.cpu().numpy(), exact)
     q_ref, s_ref = orc.quantize_rows_fp8(W)
     assert np.array_equal(orc.column_parallel_fp8(1, X, q_ref, s_ref), exact)
+
+
+def test_every_e4m3_code_exact_row_gemv():
+    """The same table through the FP8 GEMV: a row split with tp = 16 (wider than
+    a cluster).  Every shard's 256 columns hold the whole table, so every row
+    of every shard holds 448 and its scale is 1; token m is one-hot at column m
+    of shard 0, so Y[m, n] is the value of code (n + m) mod 256."""
+    vals = e4m3_table()
+    vals[0x7F], vals[0xFF] = 448.0, -448.0
+    tp, N, ks, M = 16, 256, 256, 3
+    codes = (np.arange(N)[:, None] + np.arange(ks)[None, :]) % 256
+    W = torch.from_numpy(np.tile(vals[codes], (1, tp))).to(torch.bfloat16).to(DEV)
+    X = torch.zeros(M, tp * ks, dtype=torch.bfloat16, device=DEV)
+    X[torch.arange(M), torch.arange(M)] = 1.0
+    ws, _ = shard("row", tp, W)
+    qs, ss = tpla.quantize_shards_fp8(ws)
+    torch.cuda.synchronize()
+    assert all(torch.all(sc == 1.0) for sc in ss)
+    y = tpla.row_parallel_linear_fp8(tp, X, qs, ss, None, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), vals[codes[:, :M].T])
