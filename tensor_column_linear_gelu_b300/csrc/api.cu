@@ -132,6 +132,34 @@ tp_status run(const LinearProblem& p, cudaStream_t s) {
   return fire(L, s);
 }
 
+// The prefill GEMM takes the problem (bf16, more tokens than the decode
+// kernels take).
+bool takes_gemm(const LinearProblem& p) {
+  return !p.fp8 && p.xdt == TP_BF16 && p.M > kSkinnyMaxTokens;
+}
+
+// The attention projections: QKV and O are independent (O reads the
+// caller's ctx, not the QKV output), so when both run on the prefill GEMM
+// they share one launch and neither leaves a partial last wave of tiles.
+tp_status prepare_attn_pair(const LinearProblem& qkv, const LinearProblem& o, Launch* Lq,
+                            Launch* Lo) {
+  if (takes_gemm(qkv) && takes_gemm(o)) {
+    Lo->kernel = nullptr;
+    return prepare_gemm_pair2(qkv, o, Lq);
+  }
+  const tp_status st = prepare(qkv, Lq);
+  return st != TP_OK ? st : prepare(o, Lo);
+}
+
+// Launch prepared kernels in order.
+tp_status fire_all(const Launch* L, int n, cudaStream_t s) {
+  for (int i = 0; i < n; ++i) {
+    const tp_status st = fire(L[i], s);
+    if (st != TP_OK) return st;
+  }
+  return TP_OK;
+}
+
 // Prepare every problem of a call, then launch them in order: a host-side
 // failure (a tensor map that cannot be encoded, a shape no kernel offers) is
 // reported before anything runs, so the call writes nothing.  Only a launch
@@ -677,8 +705,9 @@ tp_status tp_attn_proj(int tp, int64_t M, int64_t d_model, int n_heads, int n_kv
                               bqkv_shards, qkv_out, qkv_dt, ctx, wo_shards, bo, Y, ydt, &qkv, &o,
                               &empty);
   if (st != TP_OK || empty) return st;
-  const LinearProblem* seq[2] = {&qkv, &o};
-  return run_seq(seq, 2, reinterpret_cast<cudaStream_t>(stream));
+  thread_local Launch launches[2];
+  if ((st = prepare_attn_pair(qkv, o, &launches[0], &launches[1])) != TP_OK) return st;
+  return fire_all(launches, 2, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_layer_forward(const tp_layer_args* a, tp_stream_t stream) {
@@ -698,8 +727,11 @@ tp_status tp_layer_forward(const tp_layer_args* a, tp_stream_t stream) {
   // then that output must be in the input dtype.
   TP_RET_IF(a->X_ffn == a->Y_attn && a->attn_ydt != a->xdt, TP_ERR_DTYPE);
   if (empty_attn) return TP_OK;
-  const LinearProblem* seq[4] = {&qkv, &o, &up, &down};
-  return run_seq(seq, 4, reinterpret_cast<cudaStream_t>(stream));
+  thread_local Launch launches[4];
+  if ((st = prepare_attn_pair(qkv, o, &launches[0], &launches[1])) != TP_OK) return st;
+  if ((st = prepare(up, &launches[2])) != TP_OK) return st;
+  if ((st = prepare(down, &launches[3])) != TP_OK) return st;
+  return fire_all(launches, 4, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tp_status tp_device_status(tp_stream_t stream) {

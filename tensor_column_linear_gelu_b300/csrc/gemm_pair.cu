@@ -74,18 +74,31 @@ constexpr int64_t G = TP_GATE_UP_GROUP;
 static_assert(2 * G == PN, "a SwiGLU tile holds one gate/up group");
 static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 
-struct PairParams {
-  CUtensorMap tmA[TP_MAX_TP];  // column: [0] = X; row: X_i.  Box {64, 128}.
-  CUtensorMap tmB[TP_MAX_TP];  // W_i.  Box {64, 128}.
+// One GEMM of a launch.  A launch runs one problem, or two independent ones
+// (the attention projections: QKV and O) whose tiles share the persistent
+// grid, so the partial last wave of each is filled by the other's tiles.
+struct PairProblem {
+  int a_map, b_map;  // first tensor map of A (column: X; row: X_i) and of B (W_i) in tm[]
   const float* bias[TP_MAX_TP];
   void* Y;
-  int64_t y_extent;  // elements of Y this call may write (checked builds)
-  unsigned int* err;
+  int64_t y_extent;  // elements of Y this problem may write (checked builds)
   int64_t ldy, y_shard_stride;
   int64_t M, ns, n_out;
   int tp, row, act, ydt;
   int m_tiles, n_tiles_per_shard, n_tiles, num_tiles;
   int kb_per_shard, kb_total;
+  int tile0;         // first tile of this problem in the launch's tile sequence
+};
+constexpr int kPairMaxProblems = 2;
+// a column problem needs 1 + tp maps, a row problem 2 tp: a column and a row
+// problem together at most 1 + 3 TP_MAX_TP
+constexpr int kPairMaxMaps = 1 + 3 * TP_MAX_TP;
+
+struct PairParams {
+  CUtensorMap tm[kPairMaxMaps];  // boxes {64, 128}
+  PairProblem prob[kPairMaxProblems];
+  int nprob, num_tiles, nmaps;
+  unsigned int* err;
 };
 
 __device__ __forceinline__ int valid_count(int64_t limit, int64_t n) {
@@ -99,12 +112,19 @@ struct TileCoord {
   int64_t n0;  // first row of W_i (column) or first output column (row)
 };
 
+// The problem a tile of the launch belongs to, and its index inside it.
+__device__ __forceinline__ const PairProblem& problem_of(const PairParams& p, int tile, int& lt) {
+  const int q = (p.nprob > 1 && tile >= p.prob[1].tile0) ? 1 : 0;
+  lt = tile - p.prob[q].tile0;
+  return p.prob[q];
+}
+
 // Tiles are numbered M-fastest within groups of up to GROUP_M m-tiles, and the
 // groups are swept one after the other: the pairs running at the same time
 // share the weight tiles they stream, and a group's activations (2048 tokens)
 // stay in L2 while the weights pass through.
 constexpr int GROUP_M = 8;
-__device__ __forceinline__ TileCoord tile_coord(const PairParams& p, int tile) {
+__device__ __forceinline__ TileCoord tile_coord(const PairProblem& p, int tile) {
   const int per_group = GROUP_M * p.n_tiles;
   const int g = tile / per_group;
   const int m_first = g * GROUP_M;
@@ -160,9 +180,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    const int nmaps = p.row ? p.tp : 1;
-    for (int i = 0; i < nmaps; ++i) prefetch_tmap(&p.tmA[i]);
-    for (int i = 0; i < p.tp; ++i) prefetch_tmap(&p.tmB[i]);
+    for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.tm[i]);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), TMEM_COLS);
   // Both CTAs' barriers are initialised and the TMEM address is known before
@@ -178,10 +196,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
-      const TileCoord c = tile_coord(p, tile);
-      for (int kb = 0; kb < p.kb_total; ++kb) {
-        const int sh = p.row ? kb / p.kb_per_shard : c.shard;
-        const int kk = p.row ? kb - sh * p.kb_per_shard : kb;
+      int lt;
+      const PairProblem& P = problem_of(p, tile, lt);
+      const TileCoord c = tile_coord(P, lt);
+      for (int kb = 0; kb < P.kb_total; ++kb) {
+        const int sh = P.row ? kb / P.kb_per_shard : c.shard;
+        const int kk = P.row ? kb - sh * P.kb_per_shard : kb;
         if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs, abort_flag)) {
           report_error(p.err, kErrTimeoutProducer);
           *abort_flag = 1;
@@ -191,9 +211,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         const uint32_t fb_own = smem_u32(&full[stage]);
         const uint32_t fb = dsmem_addr(fb_own, 0);  // the even CTA's barrier
         if (lead) mbar_arrive_expect_tx(fb_own, 2 * STAGE_BYTES);
-        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &p.tmA[p.row ? sh : 0], kk * BK,
+        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &p.tm[P.a_map + (P.row ? sh : 0)], kk * BK,
                          (int)(c.m0 + (int64_t)rank * HM), fb);
-        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &p.tmB[p.row ? sh : c.shard], kk * BK,
+        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &p.tm[P.b_map + (P.row ? sh : c.shard)], kk * BK,
                          (int)(c.n0 + (int64_t)rank * HN), fb);
         if (++stage == STAGES) {
           stage = 0;
@@ -213,6 +233,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+      int lt;
+      const PairProblem& P = problem_of(p, tile, lt);
       if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
         report_error(p.err, kErrTimeoutMma);
         *abort_flag = 1;
@@ -220,7 +242,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PN);
-      for (int kb = 0; kb < p.kb_total; ++kb) {
+      for (int kb = 0; kb < P.kb_total; ++kb) {
         if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs, abort_flag)) {
           report_error(p.err, kErrTimeoutMma);
           *abort_flag = 1;
@@ -256,7 +278,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quadrant this warp may access
     const int row_in_tile = (int)rank * HM + q * 32 + lane;
-    const bool swiglu = (!p.row && p.act == TP_ACT_SWIGLU);
     const uint32_t tempty_lead = dsmem_addr(smem_u32(&tempty[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -271,14 +292,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         break;
       }
       tc_fence_after();
-      const TileCoord c = tile_coord(p, tile);
+      int lt;
+      const PairProblem& P = problem_of(p, tile, lt);
+      const bool swiglu = (!P.row && P.act == TP_ACT_SWIGLU);
+      const TileCoord c = tile_coord(P, lt);
       const int64_t m = c.m0 + row_in_tile;
-      const bool row_ok = m < p.M;
+      const bool row_ok = m < P.M;
       const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * PN);
       if (swiglu) {
         // tile = one packed group: gate columns [0,128), up columns [128,256)
         const int64_t out0 = (c.n0 / (2 * G)) * G;   // first output of the group (shard-local)
-        const int64_t base = (int64_t)c.shard * p.y_shard_stride + m * p.ldy;
+        const int64_t base = (int64_t)c.shard * P.y_shard_stride + m * P.ldy;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           float g[32], u[32];
@@ -287,14 +311,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
 #pragma unroll
           for (int j = 0; j < 32; ++j) g[j] = act_silu(g[j]) * u[j];
           const int64_t n = out0 + ch * 32;
-          const int valid = valid_count(p.ns, n);
-          if (row_ok && valid > 0 && TP_CHECK(p.err, base + n + valid <= p.y_extent))
-            store_row32(p.Y, p.ydt, base, n, valid, g);
+          const int valid = valid_count(P.ns, n);
+          if (row_ok && valid > 0 && TP_CHECK(p.err, base + n + valid <= P.y_extent))
+            store_row32(P.Y, P.ydt, base, n, valid, g);
         }
       } else {
-        const int64_t limit = p.row ? p.n_out : p.ns;
-        const int64_t base = (p.row ? 0 : (int64_t)c.shard * p.y_shard_stride) + m * p.ldy;
-        const float* bias = p.row ? p.bias[0] : p.bias[c.shard];
+        const int64_t limit = P.row ? P.n_out : P.ns;
+        const int64_t base = (P.row ? 0 : (int64_t)c.shard * P.y_shard_stride) + m * P.ldy;
+        const float* bias = P.row ? P.bias[0] : P.bias[c.shard];
 #pragma unroll 1
         for (int ch = 0; ch < PN / 32; ++ch) {
           float v[32];
@@ -306,12 +330,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
             for (int j = 0; j < 32; ++j)
               if (j < valid) v[j] += __ldg(bias + n + j);
           }
-          if (!p.row && p.act == TP_ACT_GELU_ERF) {
+          if (!P.row && P.act == TP_ACT_GELU_ERF) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = act_gelu_erf(v[j]);
           }
-          if (row_ok && valid > 0 && TP_CHECK(p.err, base + n + valid <= p.y_extent))
-            store_row32(p.Y, p.ydt, base, n, valid, v);
+          if (row_ok && valid > 0 && TP_CHECK(p.err, base + n + valid <= P.y_extent))
+            store_row32(P.Y, P.ydt, base, n, valid, v);
         }
       }
       tc_fence_before();
@@ -336,53 +360,61 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
 
 }  // namespace
 
-tp_status prepare_gemm_pair(const LinearProblem& p, Launch* L) {
-  PairParams gp{};
-  gp.err = device_error_word();
-  if (!gp.err) return TP_ERR_CUDA;
+namespace {
+
+// Fill problem q of the launch from a validated LinearProblem, encoding its
+// tensor maps from tm[*nmaps] on.
+bool fill_problem(const LinearProblem& p, PairParams& gp, int q, int* nmaps) {
+  PairProblem& P = gp.prob[q];
   const int64_t es = 2;
+  if (*nmaps + (p.row ? 2 * p.tp : 1 + p.tp) > kPairMaxMaps) return false;
+  P.a_map = *nmaps;
   if (p.row) {
     for (int i = 0; i < p.tp; ++i) {
       const void* xi = static_cast<const char*>(p.X) + (int64_t)i * p.x_shard_off * es;
-      if (!make_tma_map_bf16(&gp.tmA[i], xi, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)(p.ldx * es),
-                             HM))
-        return TP_ERR_CUDA;
+      if (!make_tma_map_bf16(&gp.tm[(*nmaps)++], xi, (uint64_t)p.K, (uint64_t)p.M,
+                             (uint64_t)(p.ldx * es), HM))
+        return false;
     }
-  } else if (!make_tma_map_bf16(&gp.tmA[0], p.X, (uint64_t)p.K, (uint64_t)p.M,
+  } else if (!make_tma_map_bf16(&gp.tm[(*nmaps)++], p.X, (uint64_t)p.K, (uint64_t)p.M,
                                 (uint64_t)(p.ldx * es), HM)) {
-    return TP_ERR_CUDA;
+    return false;
   }
+  P.b_map = *nmaps;
   for (int i = 0; i < p.tp; ++i)
-    if (!make_tma_map_bf16(&gp.tmB[i], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows,
+    if (!make_tma_map_bf16(&gp.tm[(*nmaps)++], p.W[i], (uint64_t)p.K, (uint64_t)p.w_rows,
                            (uint64_t)(p.K * es), HN))
-      return TP_ERR_CUDA;
-  for (int i = 0; i < TP_MAX_TP; ++i) gp.bias[i] = p.bias[i];
-  gp.Y = p.Y;
-  gp.ldy = p.ldy;
-  gp.y_extent = output_extent(p);
-  gp.y_shard_stride = p.y_shard_stride;
-  gp.M = p.M;
-  gp.ns = p.ns;
-  gp.n_out = p.n_out;
-  gp.tp = p.tp;
-  gp.row = p.row ? 1 : 0;
-  gp.act = p.act;
-  gp.ydt = p.ydt;
-  gp.m_tiles = (int)((p.M + PM - 1) / PM);
-  gp.kb_per_shard = (int)((p.K + BK - 1) / BK);
+      return false;
+  for (int i = 0; i < TP_MAX_TP; ++i) P.bias[i] = p.bias[i];
+  P.Y = p.Y;
+  P.ldy = p.ldy;
+  P.y_extent = output_extent(p);
+  P.y_shard_stride = p.y_shard_stride;
+  P.M = p.M;
+  P.ns = p.ns;
+  P.n_out = p.n_out;
+  P.tp = p.tp;
+  P.row = p.row ? 1 : 0;
+  P.act = p.act;
+  P.ydt = p.ydt;
+  P.m_tiles = (int)((p.M + PM - 1) / PM);
+  P.kb_per_shard = (int)((p.K + BK - 1) / BK);
   if (p.row) {
-    gp.n_tiles_per_shard = (int)((p.n_out + PN - 1) / PN);
-    gp.n_tiles = gp.n_tiles_per_shard;
-    gp.kb_total = gp.kb_per_shard * p.tp;
+    P.n_tiles_per_shard = (int)((p.n_out + PN - 1) / PN);
+    P.n_tiles = P.n_tiles_per_shard;
+    P.kb_total = P.kb_per_shard * p.tp;
   } else {
-    gp.n_tiles_per_shard = (int)((p.w_rows + PN - 1) / PN);
-    gp.n_tiles = gp.n_tiles_per_shard * p.tp;
-    gp.kb_total = gp.kb_per_shard;
+    P.n_tiles_per_shard = (int)((p.w_rows + PN - 1) / PN);
+    P.n_tiles = P.n_tiles_per_shard * p.tp;
+    P.kb_total = P.kb_per_shard;
   }
-  const int64_t tiles = (int64_t)gp.m_tiles * gp.n_tiles;
-  if (tiles > INT32_MAX) return TP_ERR_BAD_SHAPE;
-  gp.num_tiles = (int)tiles;
+  const int64_t tiles = (int64_t)P.m_tiles * P.n_tiles;
+  if (tiles > INT32_MAX / 2) return false;
+  P.num_tiles = (int)tiles;
+  return true;
+}
 
+tp_status finish_launch(PairParams& gp, Launch* L) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -390,7 +422,7 @@ tp_status prepare_gemm_pair(const LinearProblem& p, Launch* L) {
                                     SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return TP_ERR_CUDA;
-  const int pairs = (int)std::min<int64_t>(tiles, sm_count() / 2);
+  const int pairs = (int)std::min<int64_t>(gp.num_tiles, sm_count() / 2);
   L->kernel = reinterpret_cast<const void*>(gemm_pair_kernel);
   L->grid = dim3((unsigned)(2 * std::max(pairs, 1)));
   L->block = dim3(THREADS);
@@ -398,6 +430,35 @@ tp_status prepare_gemm_pair(const LinearProblem& p, Launch* L) {
   L->cluster = 2;
   L->set_params(gp);
   return TP_OK;
+}
+
+}  // namespace
+
+tp_status prepare_gemm_pair(const LinearProblem& p, Launch* L) {
+  PairParams gp{};
+  gp.err = device_error_word();
+  if (!gp.err) return TP_ERR_CUDA;
+  int nmaps = 0;
+  if (!fill_problem(p, gp, 0, &nmaps)) return TP_ERR_CUDA;
+  gp.nprob = 1;
+  gp.nmaps = nmaps;
+  gp.prob[0].tile0 = 0;
+  gp.num_tiles = gp.prob[0].num_tiles;
+  return finish_launch(gp, L);
+}
+
+tp_status prepare_gemm_pair2(const LinearProblem& a, const LinearProblem& b, Launch* L) {
+  PairParams gp{};
+  gp.err = device_error_word();
+  if (!gp.err) return TP_ERR_CUDA;
+  int nmaps = 0;
+  if (!fill_problem(a, gp, 0, &nmaps) || !fill_problem(b, gp, 1, &nmaps)) return TP_ERR_CUDA;
+  gp.nprob = 2;
+  gp.nmaps = nmaps;
+  gp.prob[0].tile0 = 0;
+  gp.prob[1].tile0 = gp.prob[0].num_tiles;
+  gp.num_tiles = gp.prob[0].num_tiles + gp.prob[1].num_tiles;
+  return finish_launch(gp, L);
 }
 
 }  // namespace tpla

@@ -103,6 +103,10 @@ tp_status prepare_gemv(const LinearProblem& p, Launch* L);
 // tcgen05 / TMEM tensor-core GEMM fed by TMA on CTA pairs (bf16; many
 // tokens; 256 x 256 tiles).
 tp_status prepare_gemm_pair(const LinearProblem& p, Launch* L);
+// Two independent problems in one launch (their tiles share the persistent
+// grid); each must be one the prefill GEMM takes, a column problem and a row
+// problem at most.
+tp_status prepare_gemm_pair2(const LinearProblem& a, const LinearProblem& b, Launch* L);
 
 // tcgen05 decode kernel with the weights as the MMA's N operand (a handful
 // of tokens, up to kSkinnyMaxTokens; bf16 weights, or e4m3 weights widened
