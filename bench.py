@@ -428,8 +428,15 @@ class Path:
                            w["hd"], qkv_out=self.qkv, Y=Y, stream=s)
 
     def launches_per_step(self):
-        return {"layer": 4, "row_ring": self.w["tp"] + 1,
-                "uneven": self.w["tp"]}.get(self.w["kind"], 2)
+        w = self.w
+        if w["kind"] == "attn" and w["M"] > 128:
+            return 1  # QKV and O share one prefill-GEMM launch
+        if w["kind"] == "layer":
+            # QKV and O share a launch when both take the prefill GEMM
+            return 3 if w["M"] > 128 else 4
+        if w["kind"] == "uneven":
+            return 1 if w["M"] <= 128 else w["tp"]
+        return {"row_ring": w["tp"] + 1}.get(w["kind"], 2)
 
 
 # Datasheet figures of one B300, for the second denominator of every
@@ -524,7 +531,7 @@ def measure(args, name, w, dev, world, steps, warmup):
         flops = sum(f for f, _ in work.values())
         nbytes = sum(b for _, b in work.values())
         dur_s = (sum(per_part["attn_proj"]) / K) / 1e3
-        launches_in_dom = 2
+        launches_in_dom = path.launches_per_step()
     bound = "tensor" if flops / nbytes > ridge else "hbm"
     long_region = elapsed_ms > 1000.0
     step_s = (elapsed_ms / K) / 1e3
