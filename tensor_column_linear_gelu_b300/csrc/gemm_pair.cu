@@ -15,16 +15,20 @@
 // Parallelism Works Under the Hood"; "Tensor parallel serving",
 // "Column-parallel and row-parallel layers, paired".)
 //
-// Structure: clusters of two CTAs (a pair), persistent over 256 x 256 output
-// tiles.  One MMA (tcgen05.mma.cta_group::2, M=256, N=256, K=16) covers the
-// pair's tile: the even CTA issues it, each CTA holds 128 of the tile's rows
+// Structure: clusters of two CTAs (a pair), one cluster per 256 x 256 output
+// tile in the grid; the clusters that run steal the tiles of those that have
+// not started (cluster launch control), so each runs many tiles.  One MMA
+// (tcgen05.mma.cta_group::2, M=256, N=256, K=16) covers the pair's tile: the
+// even CTA issues it, each CTA holds 128 of the tile's rows
 // of A (tokens) and 128 of its rows of B (weights) in shared memory, and
 // each CTA's TMEM holds the accumulator of its 128 token rows.  Per SM this
 // halves the weight bytes loaded and read per FLOP compared with a 128 x 256
 // tile on one SM.
 //   warp 0      TMA producer (both CTAs): this CTA's A and B halves of each
 //               64-wide k-block into a 6-stage ring; completion is counted on
-//               the even CTA's barrier, which expects both halves.
+//               the even CTA's barrier, which expects both halves.  The even
+//               CTA's producer also asks for the pair's next tile when it
+//               starts a tile.
 //   warp 1      TMEM allocation (both CTAs, collectively) and, in the even
 //               CTA, the single thread that issues the MMAs, committing each
 //               stage back to both producers and each finished tile to both
@@ -68,15 +72,19 @@ constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = 512;      // ACC_BUFS x PN fp32 columns
 constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
-constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
-constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+constexpr int CLC_SLOTS = 4;        // answers of the tile scheduler in flight
+// readers of each answer: both producers, the MMA thread, 8 epilogue warps
+constexpr int CLC_READERS = 2 + 1 + 8;
+constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + 2 * CLC_SLOTS;
+constexpr int SMEM_BYTES =
+    1024 /*align slack*/ + STAGES * STAGE_BYTES + CLC_SLOTS * 16 + NUM_BARS * 8 + 16;
 constexpr int64_t G = TP_GATE_UP_GROUP;
 static_assert(2 * G == PN, "a SwiGLU tile holds one gate/up group");
 static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 
 // One GEMM of a launch.  A launch runs one problem, or two independent ones
-// (the attention projections: QKV and O) whose tiles share the persistent
-// grid, so the partial last wave of each is filled by the other's tiles.
+// (the attention projections: QKV and O) whose tiles share the grid, so the
+// partial last wave of each is filled by the other's tiles.
 struct PairProblem {
   int a_map, b_map;  // first tensor map of A (column: X; row: X_i) and of B (W_i) in tm[]
   const float* bias[TP_MAX_TP];
@@ -122,7 +130,12 @@ __device__ __forceinline__ const PairProblem& problem_of(const PairParams& p, in
 // Tiles are numbered M-fastest within groups of up to GROUP_M m-tiles, and the
 // groups are swept one after the other: the pairs running at the same time
 // share the weight tiles they stream, and a group's activations (2048 tokens)
-// stay in L2 while the weights pass through.
+// stay in L2 while the weights pass through.  Tiles start in this order
+// (clusters launch, and are cancelled, in grid order), so the pairs that
+// share a weight tile start it within a few microseconds of each other and
+// the weights are read from DRAM about once per group.  Odd groups sweep the
+// n-tiles backwards, starting with the weight tiles the previous group read
+// last.
 constexpr int GROUP_M = 8;
 __device__ __forceinline__ TileCoord tile_coord(const PairProblem& p, int tile) {
   const int per_group = GROUP_M * p.n_tiles;
@@ -131,7 +144,7 @@ __device__ __forceinline__ TileCoord tile_coord(const PairProblem& p, int tile) 
   const int gm = min(GROUP_M, p.m_tiles - m_first);  // m-tiles in this group
   const int t = tile - g * per_group;
   const int mt = m_first + t % gm;
-  const int nt = t / gm;
+  const int nt = (g & 1) ? p.n_tiles - 1 - t / gm : t / gm;
   TileCoord c;
   c.m0 = (int64_t)mt * PM;
   if (p.row) {
@@ -144,18 +157,44 @@ __device__ __forceinline__ TileCoord tile_coord(const PairProblem& p, int tile) 
   return c;
 }
 
+// The pair's tile after its j-th: answer j of the scheduler (slot j mod
+// CLC_SLOTS, that slot's (j / CLC_SLOTS)-th use).  Each reader waits for the
+// answer in its own CTA, reads it, and arrives on the even CTA's cempty, so
+// the slot is asked again only once all CLC_READERS have read it.  A warp
+// calls it with every lane (whole_warp) and one arrive.  Returns the tile, -1
+// when the scheduler had nothing left, -2 when the wait gave up.
+__device__ __forceinline__ int next_tile(const uint8_t* clc_resp, uint64_t* cfull,
+                                         uint32_t cempty_lead, int j, const volatile int* abort,
+                                         bool whole_warp) {
+  const int s = j % CLC_SLOTS;
+  bool ok = mbar_wait_bounded(smem_u32(&cfull[s]), (uint32_t)(j / CLC_SLOTS) & 1u, kWaitLimitNs,
+                              abort);
+  if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return -2;
+  const int x = clc_cancelled_first_x(smem_u32(clc_resp + s * 16));
+  if (whole_warp) __syncwarp();
+  if (!whole_warp || (threadIdx.x & 31) == 0) {
+    fence_proxy_async_smem();  // the read above is ordered before the slot's next answer
+    mbar_arrive_cluster(cempty_lead + (uint32_t)(s * 8));
+  }
+  return x < 0 ? -1 : (x >> 1);
+}
+
 __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_constant__ PairParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint8_t* clc_resp = sB + STAGES * B_BYTES;  // CLC_SLOTS answers of 16 bytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(clc_resp + CLC_SLOTS * 16);
   uint64_t* full = bars;                 // even CTA's are used: both halves land there
   uint64_t* empty = bars + STAGES;       // each CTA's own: its producer waits on it
   uint64_t* tfull = bars + 2 * STAGES;   // each CTA's own: its epilogue waits on it
   uint64_t* tempty = tfull + ACC_BUFS;   // even CTA's: both epilogues arrive
   uint64_t* drain = tempty + ACC_BUFS;
+  uint64_t* cfull = drain + 1;           // each CTA's own: an answer has landed here
+  uint64_t* cempty = cfull + CLC_SLOTS;  // even CTA's: every reader of an answer arrives
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + NUM_BARS) + 1;
 
@@ -163,8 +202,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: even CTA of the pair, 1: odd
   const bool lead = rank == 0;
-  const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
+  const int own_tile = blockIdx.x >> 1;  // this cluster's tile; later ones are stolen
+  const uint32_t cempty_lead = dsmem_addr(smem_u32(&cempty[0]), 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -176,6 +215,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       mbar_init(smem_u32(&tempty[a]), 8);  // one arrive per epilogue warp of both CTAs
     }
     mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < CLC_SLOTS; ++s) {
+      mbar_init(smem_u32(&cfull[s]), 1);  // armed by this CTA's producer (16 bytes)
+      mbar_init(smem_u32(&cempty[s]), CLC_READERS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -195,7 +238,31 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+    int pending = -1;  // use of the answer slot armed here and not yet read
+    // Column problems: a group's activations stay in L2 (evict-last) while
+    // the weight tiles stream through it (evict-first); the pairs sharing a
+    // weight tile start it within a few microseconds.  Row problems keep the
+    // default policy: their tiles are long, and a weight tile's readers start
+    // it up to ~20 us apart.
+    const uint64_t pol_a = l2_policy_evict_last();
+    const uint64_t pol_b = l2_policy_evict_first();
+    int tile = own_tile;
+    for (int j = 0; tile >= 0 && ok; ++j) {
+      const int s = j % CLC_SLOTS;
+      if (lead) {
+        // ask for the next tile now: the answer is back long before this
+        // tile's loads are issued
+        if (!mbar_wait_bounded(smem_u32(&cempty[s]), ((uint32_t)(j / CLC_SLOTS) & 1u) ^ 1u,
+                               kWaitLimitNs, abort_flag)) {
+          report_error(p.err, kErrTimeoutProducer);
+          *abort_flag = 1;
+          break;
+        }
+        fence_proxy_async_smem();
+        clc_try_cancel_all(smem_u32(clc_resp + s * 16), smem_u32(&cfull[s]));
+      }
+      mbar_arrive_expect_tx(smem_u32(&cfull[s]), 16);
+      pending = j;
       int lt;
       const PairProblem& P = problem_of(p, tile, lt);
       const TileCoord c = tile_coord(P, lt);
@@ -211,16 +278,36 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         const uint32_t fb_own = smem_u32(&full[stage]);
         const uint32_t fb = dsmem_addr(fb_own, 0);  // the even CTA's barrier
         if (lead) mbar_arrive_expect_tx(fb_own, 2 * STAGE_BYTES);
-        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &p.tm[P.a_map + (P.row ? sh : 0)], kk * BK,
-                         (int)(c.m0 + (int64_t)rank * HM), fb);
-        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &p.tm[P.b_map + (P.row ? sh : c.shard)], kk * BK,
-                         (int)(c.n0 + (int64_t)rank * HN), fb);
+        const uint32_t dst_a = smem_u32(sA + stage * A_BYTES);
+        const uint32_t dst_b = smem_u32(sB + stage * B_BYTES);
+        const int ya = (int)(c.m0 + (int64_t)rank * HM);
+        const int yb = (int)(c.n0 + (int64_t)rank * HN);
+        if (P.row) {
+          tma_load_2d_pair(dst_a, &p.tm[P.a_map + sh], kk * BK, ya, fb);
+          tma_load_2d_pair(dst_b, &p.tm[P.b_map + sh], kk * BK, yb, fb);
+        } else {
+          tma_load_2d_pair_hint(dst_a, &p.tm[P.a_map], kk * BK, ya, fb, pol_a);
+          tma_load_2d_pair_hint(dst_b, &p.tm[P.b_map + c.shard], kk * BK, yb, fb, pol_b);
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      if (!ok) break;
+      tile = next_tile(clc_resp, cfull, cempty_lead, j, abort_flag, false);
+      pending = -1;
+      if (tile == -2) {
+        report_error(p.err, kErrTimeoutProducer);
+        *abort_flag = 1;
+        break;
+      }
     }
+    // An answer asked for and not read (after a failure) lands before this
+    // CTA can leave: wait for it without regard to the abort flag.
+    if (pending >= 0)
+      (void)mbar_wait_bounded(smem_u32(&cfull[pending % CLC_SLOTS]),
+                              (uint32_t)(pending / CLC_SLOTS) & 1u, kWaitLimitNs);
     // Every copy issued here is consumed by an MMA (the even CTA issues them
     // for the same tile sequence), and this CTA's epilogue waits for the
     // commit that follows the last one; the closing cluster barrier follows.
@@ -232,7 +319,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = pair; tile < p.num_tiles && ok; tile += npairs) {
+    int tile = own_tile;
+    for (int j = 0; tile >= 0 && ok; ++j) {
       int lt;
       const PairProblem& P = problem_of(p, tile, lt);
       if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
@@ -270,6 +358,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         acc = 0;
         acc_phase ^= 1u;
       }
+      tile = next_tile(clc_resp, cfull, cempty_lead, j, abort_flag, false);
+      if (tile == -2) {
+        report_error(p.err, kErrTimeoutMma);
+        *abort_flag = 1;
+        break;
+      }
     }
     // every MMA this thread issued has completed before TMEM is released
     mma_commit_pair(smem_u32(drain));
@@ -281,7 +375,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     const uint32_t tempty_lead = dsmem_addr(smem_u32(&tempty[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < p.num_tiles; tile += npairs) {
+    int tile = own_tile;
+    for (int j = 0; tile >= 0; ++j) {
       // all lanes wait, then agree: tcgen05.ld below is warp-collective, so
       // the warp must never split on a timeout
       bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, kWaitLimitNs, abort_flag);
@@ -344,6 +439,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       if (++acc == ACC_BUFS) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+      tile = next_tile(clc_resp, cfull, cempty_lead, j, abort_flag, true);
+      if (tile == -2) {
+        if (lane == 0) report_error(p.err, kErrTimeoutEpilogue);
+        *abort_flag = 1;
+        break;
       }
     }
   }
@@ -422,9 +523,10 @@ tp_status finish_launch(PairParams& gp, Launch* L) {
                                     SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return TP_ERR_CUDA;
-  const int pairs = (int)std::min<int64_t>(gp.num_tiles, sm_count() / 2);
+  // One cluster per tile: the clusters that run take over the tiles of those
+  // not yet started, in grid order.
   L->kernel = reinterpret_cast<const void*>(gemm_pair_kernel);
-  L->grid = dim3((unsigned)(2 * std::max(pairs, 1)));
+  L->grid = dim3((unsigned)(2 * std::max(gp.num_tiles, 1)));
   L->block = dim3(THREADS);
   L->smem = (size_t)SMEM_BYTES;
   L->cluster = 2;

@@ -410,6 +410,39 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Work stealing by the hardware scheduler (PTX ISA 8.6, clusterlaunchcontrol):
+// a running cluster asks to cancel the launch of a cluster of the same grid
+// that has not started, and takes over its work.  The 16-byte answer is
+// written at offset `resp` in every CTA of the cluster, and the barrier at
+// offset `bar` in each of them counts those 16 bytes (complete_tx): each
+// CTA arms its own barrier with an expect_tx of 16.
+__device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+      ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// Reads an answer: the x index of the cancelled cluster's first CTA, or -1
+// when the request cancelled nothing (every cluster of the grid has started).
+__device__ __forceinline__ int clc_cancelled_first_x(uint32_t resp) {
+  uint64_t lo, hi;
+  asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(resp) : "memory");
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "mov.b128 r, {%2, %3};\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "l"(lo), "l"(hi));
+  return ok ? (int)x : -1;
+}
+
 }  // namespace tpla
 
 namespace tpla {
