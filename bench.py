@@ -445,6 +445,11 @@ DATASHEET = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0,
              "source": "B300 datasheet: HBM3e 8 TB/s; bf16 dense 2.25 PFLOP/s"}
 
 # Decode-shaped workloads timed in the default run next to the headline one.
+KERNEL_TIMING = ("decode-shaped steps (at most 128 tokens): value from K steps with an event "
+                 "at each end of the timed region only, kernel_ms and the roofline's avg_ms "
+                 "from K further steps with an event around every launch; other steps: one "
+                 "timed pass with an event around every launch")
+PDL_MAX_TOKENS = 128  # the decode kernels' token limit: their launches overlap
 DECODE_EXTRAS = ("swiglu_ffn_decode_tp4_b1", "swiglu_ffn_decode_tp4_b8",
                  "swiglu_ffn_decode_tp4_b32", "swiglu_ffn_decode_tp4_b64",
                  "swiglu_ffn_decode_tp4_b1_fp8", "swiglu_ffn_decode_tp4_b8_fp8")
@@ -480,15 +485,41 @@ def measure(args, name, w, dev, world, steps, warmup):
 
     K = steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
+    e_first = torch.cuda.Event(enable_timing=True)
+    e_last = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index)
+    # Decode-shaped steps (at most 128 tokens: the decode kernels and GEMVs)
+    # are chains of programmatic dependent launches, and an event recorded
+    # between two launches keeps the second from overlapping the first's
+    # tail.  Their timed region has an event at each end only, and a second
+    # pass times each launch.  The prefill GEMM is launched in plain stream
+    # order: one pass, an event around every launch.
+    two_pass = flush is None and w["M"] <= PDL_MAX_TOKENS
     with clocks:
+        if two_pass:
+            # The timed region: K steps back to back with an event at each end
+            # only, so that a launch may overlap its predecessor's tail
+            # (programmatic dependent launch) as it does in use.
+            with torch.cuda.stream(s):
+                e_first.record(s)
+                for k in range(K):
+                    for _, fn in parts:
+                        fn(s)
+                e_last.record(s)
+            s.synchronize()
+            torch.cuda.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+        # Per-launch durations (the roofline's kernel): an event around every
+        # launch -- K more steps after a two-pass timed region, else the timed
+        # region itself (with a flush, the flushes outside the step events).
         with torch.cuda.stream(s):
             for k in range(K):
                 if flush is not None:
-                    flush.zero_()          # evict L2 between steps (outside the step events)
+                    flush.zero_()
                 ev[k][0].record(s)
                 for j, (_, fn) in enumerate(parts):
                     fn(s)
@@ -504,9 +535,9 @@ def measure(args, name, w, dev, world, steps, warmup):
     per_part = {pn: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(K)]
                 for j, (pn, _) in enumerate(parts)}
     step_ms = [ev[k][0].elapsed_time(ev[k][len(parts)]) for k in range(K)]
-    # Steps run back to back: with no flush the span first->last event is the
-    # timed region on the device; with a flush the flushes are excluded.
-    if flush is None:
+    if two_pass:
+        elapsed_ms = e_first.elapsed_time(e_last)
+    elif flush is None:
         elapsed_ms = ev[0][0].elapsed_time(ev[K - 1][len(parts)])
     else:
         elapsed_ms = sum(step_ms)
@@ -848,6 +879,7 @@ def main():
             "roofline": r["roofline"], "cpu_baseline": r["cpu"], "e2e": r["e2e"],
             "gpu_launches": r["launches"], "clocks": r["clocks"],
             "kernel_ms": r["per_part"],
+            "kernel_timing": KERNEL_TIMING,
         }
         if r.get("decode"):
             line["decode"] = r["decode"]

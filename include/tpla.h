@@ -300,10 +300,12 @@ tp_status column_parallel_linear_uneven(int tp, const int64_t* widths, int64_t M
  * Quantize the shards tp_shard_weights produces (for SwiGLU, the packed
  * gate/up shard: every packed row gets its own scale).  The compute calls take
  * bf16 activations and at most TP_FP8_MAX_TOKENS tokens (decode shapes: a
- * weight-streaming GEMV for one or two tokens; tensor-core kernels that widen
- * the codes exactly to bf16 on chip for more -- into tensor memory up to 64
- * tokens, into shared memory above; larger M: TP_ERR_UNSUPPORTED); K (per
- * shard for the row split) must be a multiple of 16.  The column split stays
+ * weight-streaming GEMV for one token; up to 32 tokens a tensor-core kernel
+ * that multiplies the e4m3 codes by an exact three-plane e4m3 split of each
+ * token; tensor-core kernels that widen the codes exactly to bf16 on chip for
+ * more -- into tensor memory up to 64 tokens, into shared memory above;
+ * larger M: TP_ERR_UNSUPPORTED); K (per shard for the row split) must be a
+ * multiple of 16.  The column split stays
  * bit-identical to tp = 1.
  */
 #define TP_FP8_MAX_TOKENS 128

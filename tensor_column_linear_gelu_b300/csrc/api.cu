@@ -6,6 +6,9 @@
 // same summation order whatever the shard count.
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "internal.h"
@@ -52,6 +55,45 @@ int sm_count() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+int max_active_clusters(const void* kernel, int block, int smem, int cs) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, int, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const auto key = std::make_tuple(dev, kernel, block, smem, cs);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = 0;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cs * sm_count()));
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 0) n = 0;
+  }
+  (void)cudaGetLastError();  // a refused query leaves no error behind
+  std::lock_guard<std::mutex> g(mu);
+  cache[key] = n;
+  return n;
+}
+
+void resident_clusters(const void* kernel, int block, int smem, int cs_max, int unit,
+                       int* resident) {
+  for (int c = 0; c <= cs_max; ++c) resident[c] = 0;
+  for (int c = unit; c <= cs_max; c += unit) resident[c] = max_active_clusters(kernel, block, smem, c);
 }
 
 namespace {
@@ -113,7 +155,8 @@ tp_status prepare(const LinearProblem& p, Launch* L) {
   L->kernel = nullptr;
   if (p.M == 0) return TP_OK;
   if (p.fp8) {
-    if (p.row && p.tp > kSkinnyMaxCluster) return prepare_gemv_fp8(p, L);
+    if (p.M <= kFp8GemvMaxTokens || (p.row && p.tp > kSkinnyMaxCluster))
+      return prepare_gemv_fp8(p, L);
     if (p.M <= kF8MmaMaxTokens) return prepare_f8mma(p, L);
     if (p.M <= kFp8TmemMaxTokens) return prepare_decode_fp8(p, L);
     return prepare_skinny(p, L);

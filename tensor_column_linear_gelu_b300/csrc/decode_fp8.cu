@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(TF_THREADS, 1)
     const Tile tl = row_tile(p, rank);
     const int c = tl.pc[0].c;
     const int64_t loc = tl.pc[0].loc;
-    const int w = (SK_BN + p.cs - 1) / p.cs;  // outputs per rank
+    const int w = (p.tile_cap + p.cs - 1) / p.cs;  // outputs per rank
     const int j_lo = rank * w;
     const int j_hi = (int)imin((int64_t)j_lo + w, c);
     const float* bias = p.bias[0];
@@ -608,16 +608,17 @@ tp_status prepare_decode_fp8(const LinearProblem& p, Launch* L) {
   const bool swiglu = !p.row && p.act == TP_ACT_SWIGLU;
   int tile_rows = SK_BN;
   if (p.row) {
-    // tiles of 256 outputs; tp x j CTAs per cluster, each inside one shard
-    const int64_t tiles = (p.n_out + SK_BN - 1) / SK_BN;
-    const int64_t j = std::max<int64_t>(
-        1, std::min<int64_t>({(int64_t)TF_MAX_CLUSTER / p.tp, sms / (tiles * p.tp),
-                              (int64_t)fp.kb_per_shard}));
-    const int64_t cs = p.tp * j;
-    if (tiles * cs > INT32_MAX) return TP_ERR_BAD_SHAPE;
-    fp.cs = (int)cs;
-    grid = (int)(tiles * cs);
-    fp.tile_cap = SK_BN;
+    // tiles of bn outputs; tp x j CTAs per cluster, each inside one shard
+    int resident[TF_MAX_CLUSTER + 1];
+    resident_clusters(reinterpret_cast<const void*>(fp8_tmem_kernel), TF_THREADS, TF_SMEM_MAX,
+                      TF_MAX_CLUSTER, p.tp, resident);
+    const RowTiling rt = choose_row_tiling(p.n_out, fp.kb_total, fp.kb_per_shard, sms,
+                                           TF_MAX_CLUSTER, p.tp, resident);
+    if (rt.tiles * rt.cs > INT32_MAX) return TP_ERR_BAD_SHAPE;
+    fp.cs = rt.cs;
+    grid = (int)(rt.tiles * rt.cs);
+    fp.tile_cap = rt.bn;
+    tile_rows = rt.bn;
   } else {
     const int64_t units = (fp.feat_total + SK_GRAIN - 1) / SK_GRAIN;
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, sms));

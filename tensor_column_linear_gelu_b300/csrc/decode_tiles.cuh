@@ -150,16 +150,46 @@ __device__ __forceinline__ void column_range(const P& p, int64_t& f0, int64_t& f
   column_range_of(p, (int64_t)blockIdx.x, (int64_t)gridDim.x, f0, f1);
 }
 
-// Row side: the one tile of this CTA -- its cluster's 256 outputs and its
-// rank's share of the k-blocks.
+// Row side: how the outputs are cut into tiles and each tile's K loop over a
+// cluster.  Tiles of SK_BN = 256 outputs, so that each MMA covers the most
+// weight rows it can (N = 256): these kernels run near the tensor core's
+// instruction rate, and narrower tiles measured slower per byte -- 128-wide
+// tiles on the same 128 CTAs took 121 us where 256-wide took 84 us for the
+// 8192 x 28672 down projection.  Clusters of cs CTAs split each tile's K
+// loop: cs is a multiple of cs_unit (FP8 kernels: tp, so that each CTA's
+// k-range lies inside one shard), at most cs_max, each CTA keeps at least one
+// k-block (kb_unit k-blocks per cs_unit CTAs), and the tiles' clusters fit on
+// the device at once: resident[cs] is how many clusters of cs CTAs the kernel
+// can hold (0: not known; then sms / cs).  Clusters stay inside a GPC, so
+// that is below sms / cs for cs > 2 (33 clusters of 4 on 148 SMs).  The
+// largest cs that fits wins; when none fits, cs_unit.
+struct RowTiling {
+  int bn, cs;
+  int64_t tiles;
+};
+inline RowTiling choose_row_tiling(int64_t n_out, int64_t kb_total, int64_t kb_unit, int sms,
+                                   int cs_max, int cs_unit, const int* resident) {
+  (void)kb_total;
+  const int64_t tiles = (n_out + SK_BN - 1) / SK_BN;
+  RowTiling best{SK_BN, cs_unit, tiles};
+  for (int cs = cs_unit; cs <= cs_max && cs / cs_unit <= kb_unit; cs += cs_unit) {
+    int64_t fit = resident ? resident[cs] : 0;
+    if (fit <= 0) fit = sms / cs;
+    if (tiles <= fit) best.cs = cs;
+  }
+  return best;
+}
+
+// Row side: the one tile of this CTA -- its cluster's tile_cap outputs and
+// its rank's share of the k-blocks.
 template <class P>
 TILE_FN Tile row_tile_of(const P& p, int64_t block, int rank) {
   Tile t;
   const int64_t tile = block / p.cs;
   t.n = 1;
   t.pc[0].shard = 0;
-  t.pc[0].loc = tile * SK_BN;
-  t.pc[0].c = (int)imin(SK_BN, p.feat_total - t.pc[0].loc);
+  t.pc[0].loc = tile * p.tile_cap;
+  t.pc[0].c = (int)imin(p.tile_cap, p.feat_total - t.pc[0].loc);
   t.pc[0].slot = 0;
   t.rows = (t.pc[0].c + 15) / 16 * 16;
   t.boxes = piece_boxes(t.pc[0].c);

@@ -131,14 +131,19 @@ bool make_tma_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_
                      uint64_t ld_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 
 // FP8 (e4m3) weights, bf16 activations, at most kFp8MaxTokens tokens: the
-// per-row quantizer; the weight-streaming FP8 GEMV (row-parallel calls whose
-// tp exceeds the largest cluster); the e4m3 x e4m3 kernel (M <=
-// kF8MmaMaxTokens); the FP8 decode kernel with the widened
+// per-row quantizer; the weight-streaming FP8 GEMV (one token, and
+// row-parallel calls whose tp exceeds the largest cluster); the e4m3 x e4m3
+// kernel (M <= kF8MmaMaxTokens); the FP8 decode kernel with the widened
 // weights in tensor memory (M <= kFp8TmemMaxTokens);
 // above that the shared-memory decode kernel in its FP8 mode (prepare_skinny
 // with p.fp8).
 constexpr int64_t kFp8MaxTokens = kSkinnyMaxTokens;
 constexpr int64_t kFp8TmemMaxTokens = 64;
+// One token takes the FP8 GEMV: measured on the tp=4 SwiGLU FFN (d_model
+// 8192, d_ff 28672), 87 + 49 us for the column and row launches against
+// 92 + 50 us on the e4m3 x e4m3 kernel.  (At 8 tokens the GEMV took 379 us
+// for the column: each token costs it a multiply-add per weight.)
+constexpr int64_t kFp8GemvMaxTokens = 1;
 // FP8 weights with at most this many tokens take the e4m3 x e4m3
 // tensor-core kernel: the codes stream straight into the
 // MMA's N operand and each token is split exactly into three e4m3 planes.
@@ -177,5 +182,16 @@ tp_status launch_bounded_wait_selftest(int64_t limit_ns, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// How many clusters of cs CTAs of `kernel` (block threads, smem bytes of
+// dynamic shared memory, which it sets as the kernel's maximum) the current
+// device can hold at once; 0 when the runtime cannot say.  Cached.
+int max_active_clusters(const void* kernel, int block, int smem, int cs);
+
+// resident[cs] = max_active_clusters(kernel, block, smem, cs) for the cluster
+// sizes cs = unit, 2 unit, ... up to cs_max (the others 0); resident has
+// cs_max + 1 entries.
+void resident_clusters(const void* kernel, int block, int smem, int cs_max, int unit,
+                       int* resident);
 
 }  // namespace tpla

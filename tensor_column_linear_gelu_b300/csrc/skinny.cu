@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
     const Tile tl = row_tile(p, rank);
     const int c = tl.pc[0].c;
     const int64_t loc = tl.pc[0].loc;
-    const int w = (SK_BN + p.cs - 1) / p.cs;  // outputs per rank
+    const int w = (p.tile_cap + p.cs - 1) / p.cs;  // outputs per rank
     const int j_lo = rank * w;
     const int j_hi = (int)imin((int64_t)j_lo + w, c);
     const float* bias = p.bias[0];
@@ -770,30 +770,30 @@ tp_status prepare_skinny_mode(const LinearProblem& p, Launch* L) {
   int grid = 1;
   sp.cs = 1;
   if (p.row) {
-    // Output tiles of 256; clusters of cs CTAs split each tile's K loop so
+    // Output tiles of bn; clusters of cs CTAs split each tile's K loop so
     // that tiles x cs fills the SMs (each CTA keeps at least one k-block).
-    const int64_t tiles = (p.n_out + SK_BN - 1) / SK_BN;
-    int64_t cs = std::max<int64_t>(1, std::min<int64_t>(SK_MAX_CLUSTER, sms / tiles));
-    cs = std::min<int64_t>(cs, sp.kb_total);
-    if (F8) {
-      // Each CTA's k-range must lie inside one shard (its partial is scaled
-      // by that shard's row scales): tp x j CTAs, j per shard.
-      const int64_t j = std::max<int64_t>(
-          1, std::min<int64_t>({(int64_t)SK_MAX_CLUSTER / p.tp, sms / (tiles * p.tp),
-                                (int64_t)sp.kb_per_shard}));
-      cs = p.tp * j;
-    }
-    if (tiles * cs > INT32_MAX) return TP_ERR_BAD_SHAPE;
-    sp.cs = (int)cs;
-    grid = (int)(tiles * cs);
+    // FP8 mode: each CTA's k-range lies inside one shard (its partial is
+    // scaled by that shard's row scales): tp x j CTAs, j per shard.
+    const int unit = F8 ? p.tp : 1;
+    int resident[SK_MAX_CLUSTER + 1];
+    resident_clusters(reinterpret_cast<const void*>(skinny_kernel<F8>),
+                      F8 ? SK_THREADS_F8 : SK_THREADS, SK_SMEM_MAX, SK_MAX_CLUSTER, unit, resident);
+    const decode::RowTiling rt = decode::choose_row_tiling(
+        p.n_out, sp.kb_total, F8 ? sp.kb_per_shard : sp.kb_total, sms, SK_MAX_CLUSTER, unit,
+        resident);
+    if (rt.tiles * rt.cs > INT32_MAX) return TP_ERR_BAD_SHAPE;
+    sp.cs = rt.cs;
+    sp.tile_cap = rt.bn;
+    grid = (int)(rt.tiles * rt.cs);
   } else {
     const int64_t units = (sp.feat_total + SK_GRAIN - 1) / SK_GRAIN;
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(units, sms));
   }
-  // B tile: the row side's 256 outputs; on the column side as many features
-  // (rows) as the widest CTA range, up to 256 (SwiGLU: gate + up rows).
+  // B tile: the row side's tile of outputs; on the column side as many
+  // features (rows) as the widest CTA range, up to 256 (SwiGLU: gate + up
+  // rows).
   const bool swiglu = !p.row && p.act == TP_ACT_SWIGLU;
-  int tile_rows = SK_BN;
+  int tile_rows = p.row ? sp.tile_cap : SK_BN;
   if (!p.row) {
     const int64_t units = (sp.feat_total + SK_GRAIN - 1) / SK_GRAIN;
     const int64_t max_range = (units + grid - 1) / grid * SK_GRAIN;

@@ -20,8 +20,10 @@ workload, checked against the fp64 oracle:
     bit-identical to tp=1.
   * One decoder layer's linear algebra at 8 tokens, tp=4 (64 query heads, 8
     KV heads of dim 128, SwiGLU FFN): tp_layer_forward and its CUDA-graph
-    replay, every row, against the oracle chained the same way ("What is
-    tensor parallelism?", "How a layer is split").
+    replay, every row ("What is tensor parallelism?", "How a layer is
+    split").  The projections against the oracle; the FFN bit-identical to
+    the MLP block on the layer's own attention output, and against the
+    oracle on the oracle's attention output rounded to bf16.
 Tolerances are those of gpu_helpers (bf16 inputs, fp32 output: 5e-3 x RMS).
 """
 import numpy as np
@@ -148,10 +150,26 @@ def test_layer_decode_tp4_full(orc):
     assert_close_bf16(qkv, ref_qkv)
     ref_ya = orc.o_proj(tp, a.ctx, a.Wo, None, H, hd)
     assert_h_bf16(ya, ref_ya)
+    # The layer feeds its own bf16 attention output to the FFN: its h and FFN
+    # output are those of the MLP block called on that tensor.
+    yf2, h2 = tpla.tp_mlp_block(tp, ya, w1, None, w2, None, "swiglu", d_ff=DFF,
+                                out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert_bitwise_equal(h, h2, "layer h vs MLP block on the layer's attention output")
+    assert_bitwise_equal(yf, yf2, "layer FFN output vs MLP block")
+    # The FFN against the oracle, on the oracle's attention output in bf16.  (An
+    # element of ya within rounding slack of a bf16 midpoint may round either
+    # way, which changes h there by more than half an ulp; so h is compared on
+    # the oracle's own input, not chained through ya.)
     ya_bf16 = np.vectorize(orc.round_bf16)(ref_ya)
+    x_ref = torch.tensor(ya_bf16, dtype=torch.float32).to(torch.bfloat16).to(DEV)
+    yf3, h3 = tpla.tp_mlp_block(tp, x_ref, w1, None, w2, None, "swiglu", d_ff=DFF,
+                                out_dtype=torch.float32)
+    torch.cuda.synchronize()
     ref_yf, h_exact = orc.mlp_block(tp, ya_bf16, f.W1, None, f.W2, None, "swiglu", W1u=f.W_up,
                                     round_h=False)
-    assert_h_bf16(h, h_exact)
+    assert_h_bf16(h3, h_exact)
     ref_yf, _ = orc.mlp_block(tp, ya_bf16, f.W1, None, f.W2, None, "swiglu", W1u=f.W_up,
                               round_h=True)
+    assert_close_bf16(yf3, ref_yf)
     assert_close_bf16(yf, ref_yf)

@@ -11,6 +11,10 @@
 //       piece (and half) exactly in 64- and 16-row boxes, and land inside the
 //       stage's rows; their first weight row lies inside the shard buffer;
 //   row side, every (tile, rank) of the clusters:
+//     * the cluster size the launchers choose for 256-wide tiles is in range
+//       (a multiple of the cluster unit, at most 8, at least one k-block per
+//       CTA) and the largest whose clusters all fit on the device at once,
+//       for the cluster counts measured on a B300;
 //     * tiles cover [0, N) once; ranks partition the k-blocks; with tp x j
 //       CTAs per cluster (the FP8 kernels) each rank's k-range lies in one
 //       shard.
@@ -118,21 +122,23 @@ static void check_column(const std::vector<int64_t>& widths, bool swiglu, int64_
         (long long)p.feat_total);
 }
 
-// n_out outputs, tp shards of kbs k-blocks each, clusters of cs CTAs.
-static void check_row(int64_t n_out, int tp, int kbs, int cs, bool one_shard_per_rank) {
+// n_out outputs in tiles of bn, tp shards of kbs k-blocks each, clusters of
+// cs CTAs.
+static void check_row(int64_t n_out, int tp, int kbs, int bn, int cs, bool one_shard_per_rank) {
   Params p;
   p.tp = tp;
   p.cs = cs;
+  p.tile_cap = bn;
   p.feat_total = n_out;
   p.kb_total = kbs * tp;
-  const int64_t tiles = (n_out + SK_BN - 1) / SK_BN;
+  const int64_t tiles = (n_out + bn - 1) / bn;
   int64_t covered = 0;
   for (int64_t tile = 0; tile < tiles; ++tile) {
     int next_kb = 0;
     for (int rank = 0; rank < cs; ++rank) {
       const Tile t = row_tile_of(p, tile * cs + rank, rank);
-      CHECK(t.n == 1 && t.pc[0].loc == tile * SK_BN, "tile %lld loc", (long long)tile);
-      CHECK(t.pc[0].c >= 1 && t.pc[0].c <= SK_BN && t.rows <= SK_BN, "tile %lld width",
+      CHECK(t.n == 1 && t.pc[0].loc == tile * bn, "tile %lld loc", (long long)tile);
+      CHECK(t.pc[0].c >= 1 && t.pc[0].c <= bn && t.rows <= bn, "tile %lld width",
             (long long)tile);
       CHECK(t.boxes <= SK_MAX_BOXES, "row tile boxes %d", t.boxes);
       CHECK(t.kb0 == next_kb && t.kb1 > t.kb0, "rank %d k-range [%d, %d)", rank, t.kb0, t.kb1);
@@ -146,6 +152,42 @@ static void check_row(int64_t n_out, int tp, int kbs, int cs, bool one_shard_per
   }
   CHECK(covered == n_out, "tiles cover %lld of %lld outputs", (long long)covered,
         (long long)n_out);
+}
+
+// Clusters of each size (1 .. 8 CTAs, one CTA per SM) that fit on a B300's
+// 148 SMs at once, as cudaOccupancyMaxActiveClusters reported them: clusters
+// stay inside a GPC, so sizes above 2 lose SMs to packing.
+static const int kResident[9] = {0, 148, 74, 45, 33, 26, 22, 15, 15};
+
+// The launchers' choice for n_out outputs and tp shards of kbs k-blocks:
+// bf16 kernel (cluster unit 1) and FP8 kernels (unit tp, one shard per CTA).
+static void check_choice(int64_t n_out, int tp, int kbs, bool fp8, int sms, RowTiling* out) {
+  const int unit = fp8 ? tp : 1;
+  const int64_t kb_total = (int64_t)kbs * tp;
+  const RowTiling rt =
+      choose_row_tiling(n_out, kb_total, fp8 ? kbs : kb_total, sms, 8, unit, kResident);
+  *out = rt;
+  CHECK(rt.bn == SK_BN, "bn %d", rt.bn);
+  CHECK(rt.cs % unit == 0 && rt.cs >= unit && rt.cs <= 8, "cs %d (unit %d)", rt.cs, unit);
+  CHECK(rt.tiles == (n_out + rt.bn - 1) / rt.bn, "tiles %lld", (long long)rt.tiles);
+  CHECK(rt.cs <= kb_total && (!fp8 || rt.cs / tp <= kbs), "cs %d for %d k-blocks", rt.cs, kbs);
+  // every cluster resident at once, and no larger admissible cluster would be
+  CHECK(rt.cs == unit || rt.tiles <= kResident[rt.cs], "%lld clusters of %d", (long long)rt.tiles,
+        rt.cs);
+  for (int c = rt.cs + unit; c <= 8 && c / unit <= (fp8 ? kbs : kb_total); c += unit)
+    CHECK(rt.tiles > kResident[c], "clusters of %d would fit too (cs %d chosen)", c, rt.cs);
+  check_row(n_out, tp, kbs, rt.bn, rt.cs, fp8);
+}
+
+// The down projection of the decode FFN (d_ff 28672, tp 4, d_model 8192):
+// bf16 448 k-blocks of 64, FP8 56 k-blocks of 128 per shard.  Both take 32
+// tiles x 4 CTAs (33 clusters of 4 fit; 26 of 5 would not).
+static void check_down_projection(int sms) {
+  RowTiling b, f;
+  check_choice(8192, 4, 112, false, sms, &b);
+  CHECK(b.cs == 4 && b.tiles == 32, "bf16 down projection %d x %d", b.bn, b.cs);
+  check_choice(8192, 4, 56, true, sms, &f);
+  CHECK(f.cs == 4 && f.tiles == 32, "FP8 down projection %d x %d", f.bn, f.cs);
 }
 
 int main() {
@@ -172,14 +214,24 @@ int main() {
   for (int tp = 1; tp <= 8; ++tp) check_column(std::vector<int64_t>(tp, 130 * tp + 7), true, 256, sms);
   // row side: bf16 kernel cs = min(8, 148 / tiles) (capped by the k-blocks);
   // FP8 kernels cs = tp x j
-  check_row(8192, 4, 112, 4, true);
-  check_row(8192, 8, 56, 4, false);
-  check_row(300, 1, 8, 8, true);
-  check_row(1024, 2, 16, 8, true);
-  check_row(520, 4, 4, 8, true);
-  check_row(768, 6, 8, 6, true);
-  check_row(40, 3, 1, 3, true);
-  check_row(200, 3, 8, 8, false);
+  check_row(8192, 4, 112, 256, 4, true);
+  check_row(8192, 8, 56, 256, 4, false);
+  check_row(300, 1, 8, 256, 8, true);
+  check_row(1024, 2, 16, 256, 8, true);
+  check_row(520, 4, 4, 256, 8, true);
+  check_row(768, 6, 8, 256, 6, true);
+  check_row(40, 3, 1, 256, 3, true);
+  check_row(200, 3, 8, 256, 8, false);
+  check_down_projection(sms);
+  const int64_t outs[] = {1, 16, 40, 200, 300, 520, 768, 1024, 4096, 8192, 8200, 28672};
+  const int kbss[] = {1, 2, 5, 8, 56, 112};
+  for (int64_t n : outs)
+    for (int tp = 1; tp <= 8; ++tp)
+      for (int kbs : kbss) {
+        RowTiling rt;
+        check_choice(n, tp, kbs, false, sms, &rt);
+        check_choice(n, tp, kbs, true, sms, &rt);
+      }
   if (fails) {
     std::printf("%d violation(s)\n", fails);
     return 1;
