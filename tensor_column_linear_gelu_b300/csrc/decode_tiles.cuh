@@ -151,18 +151,17 @@ __device__ __forceinline__ void column_range(const P& p, int64_t& f0, int64_t& f
 }
 
 // Row side: how the outputs are cut into tiles and each tile's K loop over a
-// cluster.  Tiles of SK_BN = 256 outputs, so that each MMA covers the most
-// weight rows it can (N = 256): these kernels run near the tensor core's
-// instruction rate, and narrower tiles measured slower per byte -- 128-wide
-// tiles on the same 128 CTAs took 121 us where 256-wide took 84 us for the
-// 8192 x 28672 down projection.  Clusters of cs CTAs split each tile's K
-// loop: cs is a multiple of cs_unit (FP8 kernels: tp, so that each CTA's
-// k-range lies inside one shard), at most cs_max, each CTA keeps at least one
-// k-block (kb_unit k-blocks per cs_unit CTAs), and the tiles' clusters fit on
-// the device at once: resident[cs] is how many clusters of cs CTAs the kernel
-// can hold (0: not known; then sms / cs).  Clusters stay inside a GPC, so
-// that is below sms / cs for cs > 2 (33 clusters of 4 on 148 SMs).  The
-// largest cs that fits wins; when none fits, cs_unit.
+// cluster.  Tiles of SK_BN = 256 outputs: narrower tiles measured slower per
+// byte -- 128-wide tiles on the same 128 CTAs took 121 us where 256-wide
+// took 84 us for the 8192 x 28672 down projection, with or without the MMAs,
+// so it is the smaller stages that cost.  Clusters of cs CTAs split each
+// tile's K loop: cs is a multiple of cs_unit (FP8 kernels: tp, so that each
+// CTA's k-range lies inside one shard), at most cs_max, each CTA keeps at
+// least one k-block (kb_unit k-blocks per cs_unit CTAs), and the tiles'
+// clusters fit on the device at once: resident[cs] is how many clusters of
+// cs CTAs the kernel can hold (0: not known; then sms / cs).  Clusters stay
+// inside a GPC, so that is below sms / cs for cs > 2 (33 clusters of 4 on
+// 148 SMs).  The largest cs that fits wins; when none fits, cs_unit.
 struct RowTiling {
   int bn, cs;
   int64_t tiles;
