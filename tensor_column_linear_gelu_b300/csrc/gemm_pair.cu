@@ -132,8 +132,8 @@ __device__ __forceinline__ const PairProblem& problem_of(const PairParams& p, in
 // share the weight tiles they stream, and a group's activations (2048 tokens)
 // stay in L2 while the weights pass through.  Tiles start in this order
 // (clusters launch, and are cancelled, in grid order), so the pairs that
-// share a weight tile start it within a few microseconds of each other and
-// the weights are read from DRAM about once per group.  Odd groups sweep the
+// share a weight tile start it within a few microseconds of each other, and
+// the weights are read from DRAM little more than once per group.  Odd groups sweep the
 // n-tiles backwards, starting with the weight tiles the previous group read
 // last.
 constexpr int GROUP_M = 8;
@@ -239,13 +239,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
     uint32_t phase = 0;
     bool ok = true;
     int pending = -1;  // use of the answer slot armed here and not yet read
-    // Column problems: a group's activations stay in L2 (evict-last) while
-    // the weight tiles stream through it (evict-first); the pairs sharing a
-    // weight tile start it within a few microseconds.  Row problems keep the
-    // default policy: their tiles are long, and a weight tile's readers start
-    // it up to ~20 us apart.
-    const uint64_t pol_a = l2_policy_evict_last();
-    const uint64_t pol_b = l2_policy_evict_first();
     int tile = own_tile;
     for (int j = 0; tile >= 0 && ok; ++j) {
       const int s = j % CLC_SLOTS;
@@ -278,17 +271,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
         const uint32_t fb_own = smem_u32(&full[stage]);
         const uint32_t fb = dsmem_addr(fb_own, 0);  // the even CTA's barrier
         if (lead) mbar_arrive_expect_tx(fb_own, 2 * STAGE_BYTES);
-        const uint32_t dst_a = smem_u32(sA + stage * A_BYTES);
-        const uint32_t dst_b = smem_u32(sB + stage * B_BYTES);
-        const int ya = (int)(c.m0 + (int64_t)rank * HM);
-        const int yb = (int)(c.n0 + (int64_t)rank * HN);
-        if (P.row) {
-          tma_load_2d_pair(dst_a, &p.tm[P.a_map + sh], kk * BK, ya, fb);
-          tma_load_2d_pair(dst_b, &p.tm[P.b_map + sh], kk * BK, yb, fb);
-        } else {
-          tma_load_2d_pair_hint(dst_a, &p.tm[P.a_map], kk * BK, ya, fb, pol_a);
-          tma_load_2d_pair_hint(dst_b, &p.tm[P.b_map + c.shard], kk * BK, yb, fb, pol_b);
-        }
+        // (One load site per operand.  Splitting them by problem kind, to give
+        // column problems L2 eviction hints, cost the row launches 6-9 %;
+        // with one site the hints changed no launch's time by more than 1 %.)
+        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &p.tm[P.a_map + (P.row ? sh : 0)], kk * BK,
+                         (int)(c.m0 + (int64_t)rank * HM), fb);
+        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &p.tm[P.b_map + (P.row ? sh : c.shard)], kk * BK,
+                         (int)(c.n0 + (int64_t)rank * HN), fb);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
