@@ -259,28 +259,34 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_pair_kernel(const __grid_cons
       int lt;
       const PairProblem& P = problem_of(p, tile, lt);
       const TileCoord c = tile_coord(P, lt);
-      for (int kb = 0; kb < P.kb_total; ++kb) {
-        const int sh = P.row ? kb / P.kb_per_shard : c.shard;
-        const int kk = P.row ? kb - sh * P.kb_per_shard : kb;
-        if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs, abort_flag)) {
-          report_error(p.err, kErrTimeoutProducer);
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        const uint32_t fb_own = smem_u32(&full[stage]);
-        const uint32_t fb = dsmem_addr(fb_own, 0);  // the even CTA's barrier
-        if (lead) mbar_arrive_expect_tx(fb_own, 2 * STAGE_BYTES);
-        // (One load site per operand.  Splitting them by problem kind, to give
-        // column problems L2 eviction hints, cost the row launches 6-9 %;
-        // with one site the hints changed no launch's time by more than 1 %.)
-        tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), &p.tm[P.a_map + (P.row ? sh : 0)], kk * BK,
-                         (int)(c.m0 + (int64_t)rank * HM), fb);
-        tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), &p.tm[P.b_map + (P.row ? sh : c.shard)], kk * BK,
-                         (int)(c.n0 + (int64_t)rank * HN), fb);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+      // The K loop as (shard, k-block in shard): a row problem walks its tp
+      // shards, a column problem its one shard's k-blocks.  This one thread
+      // issues every copy of the pair's half, two per k-block, and a k-block
+      // takes the MMAs about 0.28 us: a division per k-block to find the
+      // shard made the row launches 8-14 % slower.
+      const int nsh = P.row ? P.tp : 1;
+      const int nkk = P.row ? P.kb_per_shard : P.kb_total;
+      const int ya = (int)(c.m0 + (int64_t)rank * HM);
+      const int yb = (int)(c.n0 + (int64_t)rank * HN);
+      for (int si = 0; si < nsh && ok; ++si) {
+        const CUtensorMap* ma = &p.tm[P.a_map + (P.row ? si : 0)];
+        const CUtensorMap* mb = &p.tm[P.b_map + (P.row ? si : c.shard)];
+        for (int kk = 0; kk < nkk; ++kk) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+            report_error(p.err, kErrTimeoutProducer);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t fb_own = smem_u32(&full[stage]);
+          const uint32_t fb = dsmem_addr(fb_own, 0);  // the even CTA's barrier
+          if (lead) mbar_arrive_expect_tx(fb_own, 2 * STAGE_BYTES);
+          tma_load_2d_pair(smem_u32(sA + stage * A_BYTES), ma, kk * BK, ya, fb);
+          tma_load_2d_pair(smem_u32(sB + stage * B_BYTES), mb, kk * BK, yb, fb);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
       if (!ok) break;
