@@ -360,9 +360,14 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
             }
           }
         } else {
-          for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-            const int rsh = p.row ? kb / p.kb_per_shard : 0;  // row side: shard of this k-block
-            const int kk = p.row ? kb - rsh * p.kb_per_shard : kb;
+          // row side: shard rsh and k-block kk inside it, advanced with kb
+          int rsh = p.row ? tl.kb0 / p.kb_per_shard : 0;
+          int kk = p.row ? tl.kb0 - rsh * p.kb_per_shard : tl.kb0;
+          for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++kk) {
+            if (p.row && kk == p.kb_per_shard) {
+              kk = 0;
+              ++rsh;
+            }
             if (!waited && nd == S) flush_x();  // stage reuse needs the deferred X boxes
             bool got = true;
             if (lane == 0) got = mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u);
