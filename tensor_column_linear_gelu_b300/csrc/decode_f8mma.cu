@@ -299,7 +299,10 @@ __global__ void __launch_bounds__(FM_THREADS, 1) f8mma_kernel(const __grid_const
             if (tile_box(tl, swiglu, b, pi, hf, rr, hh)) wbytes += (uint32_t)hh * FM_ROW;
           }
         }
-        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+        const int nkb = tl.kb1 - tl.kb0;
+        const int rot = kb_rotation(nkb, p.row);
+        for (int i = 0; i < nkb; ++i) {
+          const int kb = kb_at(tl.kb0, nkb, rot, i);
           const int rsh = p.row ? kb / p.kb_per_shard : 0;
           const int kk = p.row ? kb - rsh * p.kb_per_shard : kb;
           bool got = true;
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(FM_THREADS, 1) f8mma_kernel(const __grid_const
         if (!TP_CHECK(p.err, nrows * FM_ROW <= p.w_stage_bytes &&
                                  acc * p.acc_stride + nrows <= FM_TMEM_COLS))
           ok = false;
-        for (int kb = tl.kb0; ok && kb < tl.kb1; ++kb) {
+        for (int i = 0; ok && i < tl.kb1 - tl.kb0; ++i) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase) ||
               !mbar_wait_bounded(smem_u32(&afull[stage]), phase)) {
             report_error(p.err, kErrTimeoutMma);
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(FM_THREADS, 1) f8mma_kernel(const __grid_const
 #pragma unroll
           for (int k = 0; k < FM_BK / FM_UMMA_K; ++k) {
             // K = 32 codes = 32 bytes: the start address advances by 2 x 16 bytes
-            const uint32_t accum = (kb > tl.kb0 || k > 0) ? 1u : 0u;
+            const uint32_t accum = (i > 0 || k > 0) ? 1u : 0u;
             mma_e4m3(d_tmem, adesc + (uint64_t)(k * 2), bdesc0 + (uint64_t)(k * 2), idesc0, accum);
             if (n1 > 0)
               mma_e4m3(d_tmem + SK_BN, adesc + (uint64_t)(k * 2), bdesc1 + (uint64_t)(k * 2),
@@ -688,18 +691,21 @@ __global__ void __launch_bounds__(FM_THREADS, 1) f8mma_kernel(const __grid_const
           phase ^= 1u;
         }
       };
+      // the K loop in the producer's rotated order
+      const int nkb = tl.kb1 - tl.kb0;
+      const int rot = kb_rotation(nkb, p.row);
       if (ok) {
-        load_x(tl.kb0, x0);
-        load_x(tl.kb0 + 1, x1);
+        load_x(kb_at(tl.kb0, nkb, rot, 0), x0);
+        load_x(kb_at(tl.kb0, nkb, rot, 1), x1);
       }
-      for (int kb = tl.kb0; ok && kb < tl.kb1; kb += 3) {
-        load_x(kb + 2, x2);
+      for (int i = 0; ok && i < nkb; i += 3) {
+        load_x(kb_at(tl.kb0, nkb, rot, i + 2), x2);
         convert(x0);
-        if (!ok || kb + 1 >= tl.kb1) break;
-        load_x(kb + 3, x0);
+        if (!ok || i + 1 >= nkb) break;
+        load_x(kb_at(tl.kb0, nkb, rot, i + 3), x0);
         convert(x1);
-        if (!ok || kb + 2 >= tl.kb1) break;
-        load_x(kb + 4, x1);
+        if (!ok || i + 2 >= nkb) break;
+        load_x(kb_at(tl.kb0, nkb, rot, i + 4), x1);
         convert(x2);
       }
     });

@@ -201,6 +201,27 @@ __device__ __forceinline__ Tile row_tile(const P& p, int rank) {
   return row_tile_of(p, (int64_t)blockIdx.x, rank);
 }
 
+// The e4m3 decode kernel's column side walks each tile's K loop from the
+// CTA's own starting k-block, rotating through the rest, so that the CTAs do
+// not all read the same k-offsets of their weight rows (rows a power-of-two
+// 8 KB apart) at once: its 8-token column launch went from 93.8-95.8 to
+// 90.8-91.1 us.  The rotation depends on the CTA index only, and a feature
+// belongs to the same CTA for every tp, so the column side stays
+// bit-identical to tp = 1.  Row sides (rows 7 KB apart per shard) measured
+// 2 us slower rotated, and the bf16 decode kernel (rows 16 KB apart) no
+// consistent change; both keep the plain order.
+__device__ __forceinline__ int kb_rotation(int nkb, bool row) {
+  return (nkb > 0 && !row) ? (int)(((unsigned)blockIdx.x * 37u) % (unsigned)nkb) : 0;
+}
+// k-block of iteration i (0 <= i < nkb) of a K loop [kb0, kb0 + nkb) rotated
+// by rot; kb0 + nkb (past the end) for i >= nkb.
+__device__ __forceinline__ int kb_at(int kb0, int nkb, int rot, int i) {
+  if (i >= nkb) return kb0 + nkb;
+  int j = rot + i;
+  if (j >= nkb) j -= nkb;
+  return kb0 + j;
+}
+
 // Loop over this CTA's tiles: the column side walks its feature range, the
 // row side has one tile.  Inside the body, tile_is_last tells whether tl is
 // the CTA's last tile.
