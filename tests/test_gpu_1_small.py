@@ -71,6 +71,9 @@ COLUMN_CASES = [
     (16, 256, 40000, 2, "none", torch.bfloat16, False),    # several chunks per SM
     (128, 64, 1000, 5, "none", torch.bfloat16, True),
     (6, 72, 136, 1, "swiglu", torch.bfloat16, False),
+    # prefill GEMM with more tiles (9 x 20 = 180) than clusters that run at
+    # once: the running clusters take over the others' tiles; ragged M and N
+    (2300, 256, 4100, 4, "gelu", torch.bfloat16, True),
 ]
 
 
@@ -138,6 +141,8 @@ ROW_CASES = [
     (100, 3000, 1000, 3, torch.bfloat16, True),   # K/tp = 1000: ragged k-block per shard
     (128, 1024, 4000, 2, torch.bfloat16, False),
     (5, 4096, 3000, 4, torch.bfloat16, True),
+    # prefill GEMM, 9 x 11 = 99 tiles (more than run at once), ragged M and N
+    (2300, 1024, 2600, 4, torch.bfloat16, True),
 ]
 
 
