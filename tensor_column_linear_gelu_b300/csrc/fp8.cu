@@ -283,7 +283,11 @@ tp_status prepare_fp8(const Fp8Params& gp, Launch* L) {
 template <int ACT, bool ROW>
 tp_status dispatch_fp8_mt(const Fp8Params& gp, Launch* L) {
   constexpr bool SW = (ACT == TP_ACT_SWIGLU);
-  if (gp.M <= 1) return prepare_fp8<1, SW ? 2 : 4, 2, ACT, ROW>(gp, L);
+  // one token: a SwiGLU column warp takes one output (its gate and up rows)
+  // with four 16-byte loads per row in flight -- 81 us against 87 us with two
+  // outputs and two loads; the row and the other columns keep four outputs
+  // (fewer made the row launch slower: 65 against 47 us)
+  if (gp.M <= 1) return prepare_fp8<1, SW ? 1 : 4, 4, ACT, ROW>(gp, L);
   if (gp.M <= 2) return prepare_fp8<2, SW ? 2 : 4, 2, ACT, ROW>(gp, L);
   if (gp.M <= 4) return prepare_fp8<4, SW ? 2 : 4, 1, ACT, ROW>(gp, L);
   return prepare_fp8<8, SW ? 2 : 4, 1, ACT, ROW>(gp, L);
