@@ -64,8 +64,12 @@ __global__ void __launch_bounds__(QTHREADS) quantize_fp8_rows_kernel(
 }
 
 // ---------------------------------------------------------------- GEMV
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+// Warps per block: one for a single token -- 32-thread blocks spread the
+// warps evenly over the SMs (one-token SwiGLU FFN, tp 4: column 81 against
+// 83 us, step 128 against 130 us; 2- and 4-warp blocks were slower than 8);
+// eight for more tokens.
+template <int MT>
+constexpr int warps_of() { return MT == 1 ? 1 : 8; }
 constexpr int E = 16;  // weights per 16-byte vector
 
 struct Fp8Params {
@@ -139,7 +143,8 @@ __device__ __forceinline__ void accumulate_fp8(float (&acc)[MT][NR], const uint8
 }
 
 template <int MT, int R, int U, int ACT, bool ROW>
-__global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constant__ Fp8Params p) {
+__global__ void __launch_bounds__(warps_of<MT>() * 32) gemv_fp8_kernel(const __grid_constant__ Fp8Params p) {
+  constexpr int kWarps = warps_of<MT>();
   constexpr bool SW = (ACT == TP_ACT_SWIGLU);
   constexpr int NR = SW ? 2 * R : R;
   constexpr int64_t G = TP_GATE_UP_GROUP;
@@ -258,6 +263,8 @@ __global__ void __launch_bounds__(kThreads) gemv_fp8_kernel(const __grid_constan
 template <int MT, int R, int U, int ACT, bool ROW>
 tp_status prepare_fp8(const Fp8Params& gp, Launch* L) {
   auto kern = gemv_fp8_kernel<MT, R, U, ACT, ROW>;
+  constexpr int kWarps = warps_of<MT>();
+  constexpr int kThreads = kWarps * 32;
   static int resident = 0;
   static std::once_flag once;
   std::call_once(once, [&] {
