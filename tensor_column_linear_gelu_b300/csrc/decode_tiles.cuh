@@ -161,22 +161,43 @@ __device__ __forceinline__ void column_range(const P& p, int64_t& f0, int64_t& f
 // clusters fit on the device at once: resident[cs] is how many clusters of
 // cs CTAs the kernel can hold (0: not known; then sms / cs).  Clusters stay
 // inside a GPC, so that is below sms / cs for cs > 2 (33 clusters of 4 on
-// 148 SMs).  The largest cs that fits wins; when none fits, cs_unit.
+// 148 SMs).  The largest cs that fits wins; when none fits, cs_unit.  The
+// bf16 decode kernel's column side uses the same choice for its K-split
+// tiles (bn features each).
 struct RowTiling {
   int bn, cs;
   int64_t tiles;
 };
 inline RowTiling choose_row_tiling(int64_t n_out, int64_t kb_total, int64_t kb_unit, int sms,
-                                   int cs_max, int cs_unit, const int* resident) {
+                                   int cs_max, int cs_unit, const int* resident,
+                                   int bn = SK_BN) {
   (void)kb_total;
-  const int64_t tiles = (n_out + SK_BN - 1) / SK_BN;
-  RowTiling best{SK_BN, cs_unit, tiles};
+  const int64_t tiles = (n_out + bn - 1) / bn;
+  RowTiling best{bn, cs_unit, tiles};
   for (int cs = cs_unit; cs <= cs_max && cs / cs_unit <= kb_unit; cs += cs_unit) {
     int64_t fit = resident ? resident[cs] : 0;
     if (fit <= 0) fit = sms / cs;
     if (tiles <= fit) best.cs = cs;
   }
   return best;
+}
+
+// Column side with the K loop split over clusters (bf16 decode kernel, when
+// the feature walk would leave each CTA too few weight rows to keep the
+// tensor core's fixed cost per MMA hidden): cluster `block / cs` owns the
+// features [tile * tile_cap, (tile + 1) * tile_cap) and its CTA of rank r
+// the k-blocks [r * kb_total / cs, (r + 1) * kb_total / cs) of each tile that
+// covers them.
+template <class P>
+TILE_FN void column_split_range_of(const P& p, int64_t block, int64_t& f0, int64_t& f1) {
+  const int64_t tile = block / p.cs;
+  f0 = imin(tile * p.tile_cap, p.feat_total);
+  f1 = imin(f0 + p.tile_cap, p.feat_total);
+}
+template <class P>
+TILE_FN void split_kb_range(const P& p, int rank, int& kb0, int& kb1) {
+  kb0 = (int)((int64_t)rank * p.kb_total / p.cs);
+  kb1 = (int)((int64_t)(rank + 1) * p.kb_total / p.cs);
 }
 
 // Row side: the one tile of this CTA -- its cluster's tile_cap outputs and

@@ -24,9 +24,17 @@
 //                     packed at 16-row slots into one B tile of up to 512
 //                     weight rows (two MMAs of N <= 256 per k-step), so a CTA
 //                     normally runs a single K loop with every stage full.  Every
-//                     output accumulates over all of K in one TMEM column --
-//                     no split-K -- so its summation order depends on K only
-//                     and sharded results are bit-identical to tp = 1.
+//                     output accumulates over all of K in one TMEM column,
+//                     so its summation order depends on K only and sharded
+//                     results are bit-identical to tp = 1.
+//                     With fewer than SK_SPLIT_ROWS weight rows per CTA the
+//                     walk is bound by the fixed cost of each MMA instead:
+//                     then clusters of cs CTAs take 256-row tiles (features
+//                     [t*256, (t+1)*256), SwiGLU 128 gate + 128 up) and split
+//                     the K loop, and their partials are summed in rank order
+//                     as on the row side below.  The choice depends on F, K,
+//                     M and the SM count, not on the shards, so tp = 1 makes
+//                     the same one and the results stay bit-identical.
 //                     SwiGLU: a piece's gate rows sit at its slot among the
 //                     tile's first R rows and its up rows at the same slot
 //                     among the next R (R = slot rows of the tile, <= 256);
@@ -107,6 +115,26 @@ namespace {
 
 using namespace decode;
 
+// This kernel's tile loop: the shared one, with a column tile's K loop
+// narrowed to the CTA's k-blocks [skb0, skb1) (all of K unless clusters
+// split K).
+#undef SK_FOR_EACH_TILE
+#define SK_FOR_EACH_TILE(tl, ...)                                     \
+  do {                                                                \
+    if (p.row) {                                                      \
+      const Tile tl = row_tile(p, rank);                              \
+      __VA_ARGS__                                                     \
+    } else {                                                          \
+      for (int64_t f_ = f0; f_ < f1;) {                               \
+        Tile t_ = column_tile(p, f_, f1);                             \
+        t_.kb0 = skb0;                                                \
+        t_.kb1 = skb1;                                                \
+        const Tile tl = t_;                                           \
+        __VA_ARGS__                                                   \
+      }                                                               \
+    }                                                                 \
+  } while (0)
+
 constexpr int SK_THREADS = 192;
 constexpr int SK_EPI_WARP0 = 2;
 constexpr int SK_CONV_WARP0 = 6;            // FP8 mode: first converter warp
@@ -140,6 +168,20 @@ constexpr int SK_RED_PITCH = SK_BN + 4;     // floats per token row of a reducti
 constexpr int SK_NUM_BARS = 4 * SK_MAX_STAGES + 2 * SK_ACC_BUFS + 1 + 2 * SK_MAX_CSTAGES;
 constexpr int SK_BAR_BYTES = SK_NUM_BARS * 8 + 16;
 constexpr int SK_SMEM_MAX = 232448;         // dynamic shared memory per CTA (227 KB)
+// Column side: below this many weight rows per CTA the feature walk is bound
+// by the tensor core's fixed time per MMA (about 140 cycles, whatever N):
+// the 8-token QKV projection (80 rows a CTA) took 0.43 us a k-block, 73 us
+// for 168 MB.  Such calls give each cluster of cs CTAs a 256-row tile and
+// split its K loop instead (partials summed in rank order, as on the row
+// side), for up to SK_SPLIT_MAX_TOKENS tokens (the partial-sum buffer sits
+// beside the ring), with at least SK_SPLIT_MIN_KB k-blocks per CTA: short
+// K loops are not MMA-bound, and there the clusters' fixed costs lose (the
+// [16, 512] x 2048 GELU up projection, 8 k-blocks, went from 22 to 60 us
+// split 8 ways).  The choice depends on the total feature count, K, M and
+// the SM count only, so sharded results stay bit-identical to tp = 1.
+constexpr int SK_SPLIT_ROWS = 128;
+constexpr int SK_SPLIT_MAX_TOKENS = 32;
+constexpr int SK_SPLIT_MIN_KB = 32;
 
 struct SkinnyParams {
   CUtensorMap tmX[TP_MAX_TP];    // column: [0] = X; row: X_i.  Box {64, xrows}.
@@ -163,8 +205,10 @@ struct SkinnyParams {
   int tile_cap;                  // column: features (SwiGLU) or rows per tile
   int acc_stride, acc_bufs;      // TMEM columns per accumulator buffer, buffers
   int kb_per_shard, kb_total;
-  int cs;                        // row side: CTAs per cluster splitting K
+  int cs;                        // CTAs per cluster splitting K (row side, column K split)
+  int csplit;                    // column side: clusters of cs CTAs split each tile's K loop
   int ring_bytes;                // shared memory below the barriers (checked builds)
+  int red_off, red_bytes;        // column K split: the partial-sum buffer in shared memory
 };
 
 template <bool F8>
@@ -195,12 +239,12 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + SK_NUM_BARS);
   // Row side: after the K loop the ring is reused as this CTA's reduction
   // buffer red[token][SK_RED_PITCH] (fp32).
-  float* red = reinterpret_cast<float*>(smem);
+  float* red = reinterpret_cast<float*>(smem + p.red_off);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool swiglu = (!p.row && p.act == TP_ACT_SWIGLU);
-  const int rank = p.row ? (int)cluster_ctarank() : 0;
+  const int rank = (p.row || p.csplit) ? (int)cluster_ctarank() : 0;
   // row side, FP8 mode: the shard this CTA's k-range lies in
   const int rshard = p.row ? (int)((int64_t)rank * p.tp / p.cs) : 0;
   // The next kernel may start its prologue now.  The producer waits for the
@@ -247,7 +291,12 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   int64_t f0 = 0, f1 = 0;
-  if (!p.row) column_range(p, f0, f1);
+  if (p.csplit)
+    column_split_range_of(p, (int64_t)blockIdx.x, f0, f1);
+  else if (!p.row)
+    column_range(p, f0, f1);
+  int skb0 = 0, skb1 = p.kb_total;  // column side: this CTA's k-blocks
+  if (p.csplit) split_kb_range(p, rank, skb0, skb1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -503,7 +552,35 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
         // loads: no arithmetic and no stores.  Accumulator columns are read
         // 16 (gate and up: 2 x 16) at a time with one wait.
         const bool live = t < p.M;
-        if (has_tokens && p.row && p.cs > 1) {
+        if (has_tokens && p.csplit) {
+          // column K split: this rank's partials of the cluster's features
+          // -> shared memory, at the feature's offset in the cluster's range
+          // (SwiGLU: up partials tile_cap further)
+          for (int i = 0; i < tl.n; ++i) {
+            const Piece& pc = tl.pc[i];
+            const int64_t fl0 = p.fo[pc.shard] + pc.loc - f0;
+#pragma unroll 1
+            for (int j0 = 0; j0 < pc.c; j0 += 16) {
+              float v[16], u[16];
+              const uint32_t tg = taddr + (uint32_t)(pc.slot + j0);
+              if (swiglu)
+                tmem_ld16x2(tg, taddr + (uint32_t)(tl.rows + pc.slot + j0), v, u);
+              else
+                tmem_ld16(tg, v);
+              if (!live) continue;
+              const int valid = pc.c - j0 < 16 ? pc.c - j0 : 16;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int64_t o = t * SK_RED_PITCH + fl0 + j0 + j;
+                if (j < valid &&
+                    TP_CHECK(p.err, (o + (swiglu ? p.tile_cap : 0) + 1) * 4 <= p.red_bytes)) {
+                  red[o] = v[j];
+                  if (swiglu) red[o + p.tile_cap] = u[j];
+                }
+              }
+            }
+          }
+        } else if (has_tokens && p.row && p.cs > 1) {
           // this rank's partial sum -> shared memory, for the cluster reduction
           const int c = tl.pc[0].c;
 #pragma unroll 1
@@ -708,6 +785,45 @@ __global__ void __launch_bounds__(F8 ? SK_THREADS_F8 : SK_THREADS, 1)
     }
     cluster_sync_all();  // no CTA leaves while a peer still reads its buffer
   }
+  if (p.csplit) {
+    // ---------------------------------------------- column K split: reduction
+    // CTA r of the cluster finishes features [r w, (r + 1) w) of its range:
+    // the cs partials in rank order, then bias / activation, one rounding.
+    // Every thread of every CTA passes both barriers.
+    cluster_sync_all();
+    const int64_t nf = f1 - f0;
+    const int64_t w = (nf + p.cs - 1) / p.cs;
+    const int64_t lo = (int64_t)rank * w;
+    const int64_t hi = imin(lo + w, nf);
+    const uint32_t red_s = smem_u32(red);
+    if (hi > lo) {
+      const int64_t span = hi - lo;
+      const int64_t items = p.M * span;
+      for (int64_t it = threadIdx.x; it < items; it += blockDim.x) {
+        const int64_t tok = it / span;
+        const int64_t fl = lo + (it - tok * span);
+        const int64_t g = f0 + fl;
+        int sh = 0;
+        while (sh + 1 < p.tp && p.fo[sh + 1] <= g) ++sh;
+        const int64_t loc = g - p.fo[sh];
+        const uint32_t off = (uint32_t)((tok * SK_RED_PITCH + fl) * 4);
+        float v = 0.0f;
+        for (int r = 0; r < p.cs; ++r) v += dsmem_ld_f32(dsmem_addr(red_s + off, (uint32_t)r));
+        if (swiglu) {
+          const uint32_t offu = off + (uint32_t)(p.tile_cap * 4);
+          float u = 0.0f;
+          for (int r = 0; r < p.cs; ++r) u += dsmem_ld_f32(dsmem_addr(red_s + offu, (uint32_t)r));
+          v = act_silu(v) * u;
+        } else {
+          if (p.bias[sh]) v += __ldg(p.bias[sh] + loc);
+          if (p.act == TP_ACT_GELU_ERF) v = act_gelu_erf(v);
+        }
+        const int64_t yo = p.yoff[sh] + tok * p.ldy + loc;
+        if (TP_CHECK(p.err, yo < p.y_extent)) store_out(p.Y, p.ydt, yo, v);
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while a peer still reads its buffer
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -774,13 +890,14 @@ tp_status prepare_skinny_mode(const LinearProblem& p, Launch* L) {
   const int sms = sm_count();
   int grid = 1;
   sp.cs = 1;
+  sp.csplit = 0;
+  int resident[SK_MAX_CLUSTER + 1];
   if (p.row) {
     // Output tiles of bn; clusters of cs CTAs split each tile's K loop so
     // that tiles x cs fills the SMs (each CTA keeps at least one k-block).
     // FP8 mode: each CTA's k-range lies inside one shard (its partial is
     // scaled by that shard's row scales): tp x j CTAs, j per shard.
     const int unit = F8 ? p.tp : 1;
-    int resident[SK_MAX_CLUSTER + 1];
     resident_clusters(reinterpret_cast<const void*>(skinny_kernel<F8>),
                       F8 ? SK_THREADS_F8 : SK_THREADS, SK_SMEM_MAX, SK_MAX_CLUSTER, unit, resident);
     const decode::RowTiling rt = decode::choose_row_tiling(
@@ -806,13 +923,34 @@ tp_status prepare_skinny_mode(const LinearProblem& p, Launch* L) {
     const int64_t cap = (F8 && swiglu) ? SK_BN / 2 : SK_BN;
     sp.tile_cap = (int)std::min<int64_t>(cap, max_range);
     tile_rows = swiglu ? 2 * sp.tile_cap : sp.tile_cap;
+    if (!F8 && tile_rows < SK_SPLIT_ROWS && p.M <= SK_SPLIT_MAX_TOKENS) {
+      // K split over clusters: tiles of 256 weight rows (SwiGLU: 128
+      // features, gate and up)
+      const int wf = swiglu ? SK_BN / 2 : SK_BN;
+      resident_clusters(reinterpret_cast<const void*>(skinny_kernel<F8>), SK_THREADS,
+                        SK_SMEM_MAX, SK_MAX_CLUSTER, 1, resident);
+      const decode::RowTiling ct = decode::choose_row_tiling(
+          sp.feat_total, sp.kb_total, sp.kb_total / SK_SPLIT_MIN_KB, sms, SK_MAX_CLUSTER, 1,
+          resident, wf);
+      if (ct.cs >= 2 && ct.tiles * ct.cs <= INT32_MAX) {
+        sp.csplit = 1;
+        sp.cs = ct.cs;
+        sp.tile_cap = wf;
+        tile_rows = swiglu ? 2 * wf : wf;
+        grid = (int)(ct.tiles * ct.cs);
+      }
+    }
   }
   sp.w_stage_bytes = tile_rows * SK_ROW_BYTES;
   sp.raw_stage_bytes = F8 ? tile_rows * SK_RAW_ROW_BYTES : 0;
   sp.cstages = F8 ? SK_CSTAGES : 0;
   sp.acc_stride = (tile_rows + 31) / 32 * 32;
   sp.acc_bufs = (SK_ACC_BUFS * sp.acc_stride <= SK_TMEM_COLS) ? SK_ACC_BUFS : 1;
-  const int avail = SK_SMEM_MAX - 1024 - SK_BAR_BYTES;
+  // column K split: the partial sums of up to SK_SPLIT_MAX_TOKENS tokens,
+  // after the barriers
+  const int bar_bytes = (SK_BAR_BYTES + 15) / 16 * 16;
+  sp.red_bytes = sp.csplit ? (int)p.M * SK_RED_PITCH * 4 : 0;
+  const int avail = SK_SMEM_MAX - 1024 - bar_bytes - sp.red_bytes;
   // bf16: a stage is the X box and the weight rows.  FP8: a stage is the raw
   // codes; the X ring (about 32 KB) and the bf16 buffers are fixed.
   sp.xstages = F8 ? std::max(2, std::min(SK_MAX_STAGES, 32768 / sp.x_stage_bytes)) : 0;
@@ -830,7 +968,8 @@ tp_status prepare_skinny_mode(const LinearProblem& p, Launch* L) {
   // the ring.
   if ((x_ring_stages - 1) * sp.x_stage_bytes + SK_A_BYTES > ring) return TP_ERR_UNSUPPORTED;
   if (p.row && sp.cs > 1 && (int64_t)xrows * SK_RED_PITCH * 4 > ring) return TP_ERR_UNSUPPORTED;
-  const int smem = 1024 + ring + SK_BAR_BYTES;
+  sp.red_off = sp.csplit ? ring + bar_bytes : 0;
+  const int smem = 1024 + ring + bar_bytes + sp.red_bytes;
 
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;

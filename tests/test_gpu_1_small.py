@@ -71,6 +71,13 @@ COLUMN_CASES = [
     (16, 256, 40000, 2, "none", torch.bfloat16, False),    # several chunks per SM
     (128, 64, 1000, 5, "none", torch.bfloat16, True),
     (6, 72, 136, 1, "swiglu", torch.bfloat16, False),
+    # decode column launches with too few weight rows per SM and long K
+    # loops split K over clusters: ten 20-feature shards need two tiles per
+    # cluster range; a gate/up tile of 128 features runs across a shard
+    # boundary
+    (8, 4096, 200, 10, "gelu", torch.bfloat16, True),
+    (12, 4096, 360, 3, "swiglu", torch.bfloat16, False),
+    (32, 8192, 2560, 4, "none", torch.bfloat16, False),
     # prefill GEMM with more tiles (9 x 20 = 180) than clusters that run at
     # once: the running clusters take over the others' tiles; ragged M and N
     (2300, 256, 4100, 4, "gelu", torch.bfloat16, True),

@@ -10,6 +10,16 @@
 //     * the boxes tile_box enumerates are at most SK_MAX_BOXES, cover each
 //       piece (and half) exactly in 64- and 16-row boxes, and land inside the
 //       stage's rows; their first weight row lies inside the shard buffer;
+//   column side with K split over clusters (bf16 decode kernel, when the
+//   feature walk leaves fewer than 128 weight rows a CTA), every CTA:
+//     * the split is chosen from the total feature count, K and the SM count
+//       only (so tp = 1 takes the same one), cs >= 2 clusters all resident,
+//       at least 32 k-blocks per CTA;
+//     * the clusters' feature ranges partition [0, F) in tiles of 256
+//       features (SwiGLU 128); ranks partition each tile's k-blocks;
+//     * each CTA's tiles cover its range with the checks above, and every
+//       feature's partial-sum slot (SwiGLU: gate and up) lies inside the
+//       260-float row of the reduction buffer;
 //   row side, every (tile, rank) of the clusters:
 //     * the cluster size the launchers choose for 256-wide tiles is in range
 //       (a multiple of the cluster unit, at most 8, at least one k-block per
@@ -48,6 +58,57 @@ static int fails = 0;
 
 static int64_t gate_up_rows(int64_t ns) { return 2 * G * ((ns + G - 1) / G); }
 
+// A CTA's walk over its features [f0, f1): the tiles column_tile cuts.
+static void walk_tiles(const Params& p, const std::vector<int64_t>& widths, bool swiglu,
+                       int tile_rows, int64_t f0, int64_t f1) {
+  for (int64_t f = f0; f < f1;) {
+    const int64_t start = f;
+    const Tile t = column_tile(p, f, f1);
+    CHECK(t.n >= 1 && f > start, "no progress at feature %lld", (long long)start);
+    CHECK(t.rows <= p.tile_cap, "tile rows %d > cap %d", t.rows, p.tile_cap);
+    CHECK(t.boxes <= SK_MAX_BOXES, "%d boxes", t.boxes);
+    int64_t g = start;
+    int slot = 0, boxes = 0;
+    for (int i = 0; i < t.n; ++i) {
+      const Piece& pc = t.pc[i];
+      CHECK(pc.slot == slot && pc.slot % 16 == 0, "piece %d slot %d, expected %d", i, pc.slot,
+            slot);
+      CHECK(pc.c >= 1, "empty piece");
+      CHECK(p.fo[pc.shard] <= g && g < p.fo[pc.shard + 1], "piece %d in the wrong shard", i);
+      CHECK(pc.loc == g - p.fo[pc.shard], "piece %d loc", i);
+      CHECK(pc.loc + pc.c <= widths[pc.shard], "piece %d crosses its shard's end", i);
+      if (swiglu) CHECK(pc.loc / G == (pc.loc + pc.c - 1) / G, "piece %d crosses a group", i);
+      const int64_t buf_rows = swiglu ? gate_up_rows(widths[pc.shard]) : widths[pc.shard];
+      // this piece's boxes, in tile_box order
+      for (int half = 0; half < (swiglu ? 2 : 1); ++half) {
+        int covered = 0;
+        while (covered < pc.c) {
+          int pi, hf, r, h;
+          CHECK(tile_box(t, swiglu, boxes, pi, hf, r, h), "box %d missing", boxes);
+          CHECK(pi == i && hf == half && r == covered, "box %d is (%d,%d,%d)", boxes, pi, hf, r);
+          CHECK(h == 64 || h == 16, "box height %d", h);
+          CHECK(pc.slot + half * t.rows + r + h <= tile_rows, "box %d leaves the stage", boxes);
+          const int64_t wrow =
+              (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G + half * G : pc.loc) + r;
+          CHECK(wrow < buf_rows, "box %d starts at weight row %lld of %lld", boxes,
+                (long long)wrow, (long long)buf_rows);
+          covered += h;
+          ++boxes;
+        }
+        CHECK(covered == (pc.c + 15) / 16 * 16 || (covered >= pc.c && covered - pc.c < 16),
+              "piece %d half %d covered %d rows for %d", i, half, covered, pc.c);
+      }
+      g += pc.c;
+      slot += (pc.c + 15) / 16 * 16;
+    }
+    int pi, hf, r, h;
+    CHECK(!tile_box(t, swiglu, boxes, pi, hf, r, h) && boxes == t.boxes, "box count %d vs %d",
+          boxes, t.boxes);
+    CHECK(g == f && slot == t.rows, "tile covers [%lld, %lld), advanced to %lld",
+          (long long)start, (long long)g, (long long)f);
+  }
+}
+
 // widths: per-shard features; swiglu; cap_features: the launcher's cap.
 static void check_column(const std::vector<int64_t>& widths, bool swiglu, int64_t cap_limit,
                          int sms) {
@@ -71,52 +132,8 @@ static void check_column(const std::vector<int64_t>& widths, bool swiglu, int64_
     CHECK(f0 % SK_GRAIN == 0 && f1 >= f0, "CTA %lld range [%lld, %lld)", (long long)b,
           (long long)f0, (long long)f1);
     expect = f1;
-    for (int64_t f = f0; f < f1;) {
-      const int64_t start = f;
-      const Tile t = column_tile(p, f, f1);
-      CHECK(t.n >= 1 && f > start, "no progress at feature %lld", (long long)start);
-      CHECK(t.rows <= p.tile_cap, "tile rows %d > cap %d", t.rows, p.tile_cap);
-      CHECK(t.boxes <= SK_MAX_BOXES, "%d boxes", t.boxes);
-      int64_t g = start;
-      int slot = 0, boxes = 0;
-      for (int i = 0; i < t.n; ++i) {
-        const Piece& pc = t.pc[i];
-        CHECK(pc.slot == slot && pc.slot % 16 == 0, "piece %d slot %d, expected %d", i, pc.slot,
-              slot);
-        CHECK(pc.c >= 1, "empty piece");
-        CHECK(p.fo[pc.shard] <= g && g < p.fo[pc.shard + 1], "piece %d in the wrong shard", i);
-        CHECK(pc.loc == g - p.fo[pc.shard], "piece %d loc", i);
-        CHECK(pc.loc + pc.c <= widths[pc.shard], "piece %d crosses its shard's end", i);
-        if (swiglu) CHECK(pc.loc / G == (pc.loc + pc.c - 1) / G, "piece %d crosses a group", i);
-        const int64_t buf_rows = swiglu ? gate_up_rows(widths[pc.shard]) : widths[pc.shard];
-        // this piece's boxes, in tile_box order
-        for (int half = 0; half < (swiglu ? 2 : 1); ++half) {
-          int covered = 0;
-          while (covered < pc.c) {
-            int pi, hf, r, h;
-            CHECK(tile_box(t, swiglu, boxes, pi, hf, r, h), "box %d missing", boxes);
-            CHECK(pi == i && hf == half && r == covered, "box %d is (%d,%d,%d)", boxes, pi, hf, r);
-            CHECK(h == 64 || h == 16, "box height %d", h);
-            CHECK(pc.slot + half * t.rows + r + h <= tile_rows, "box %d leaves the stage", boxes);
-            const int64_t wrow =
-                (swiglu ? (pc.loc / G) * 2 * G + pc.loc % G + half * G : pc.loc) + r;
-            CHECK(wrow < buf_rows, "box %d starts at weight row %lld of %lld", boxes,
-                  (long long)wrow, (long long)buf_rows);
-            covered += h;
-            ++boxes;
-          }
-          CHECK(covered == (pc.c + 15) / 16 * 16 || (covered >= pc.c && covered - pc.c < 16),
-                "piece %d half %d covered %d rows for %d", i, half, covered, pc.c);
-        }
-        g += pc.c;
-        slot += (pc.c + 15) / 16 * 16;
-      }
-      int pi, hf, r, h;
-      CHECK(!tile_box(t, swiglu, boxes, pi, hf, r, h) && boxes == t.boxes, "box count %d vs %d",
-            boxes, t.boxes);
-      CHECK(g == f && slot == t.rows, "tile covers [%lld, %lld), advanced to %lld",
-            (long long)start, (long long)g, (long long)f);
-    }
+    walk_tiles(p, widths, swiglu, tile_rows, f0, f1);
+    if (fails) return;
   }
   CHECK(expect == p.feat_total, "ranges end at %lld of %lld", (long long)expect,
         (long long)p.feat_total);
@@ -158,6 +175,72 @@ static void check_row(int64_t n_out, int tp, int kbs, int bn, int cs, bool one_s
 // 148 SMs at once, as cudaOccupancyMaxActiveClusters reported them: clusters
 // stay inside a GPC, so sizes above 2 lose SMs to packing.
 static const int kResident[9] = {0, 148, 74, 45, 33, 26, 22, 15, 15};
+
+// Column side with the K loop split over clusters, as the bf16 decode
+// kernel's launcher sets it up: returns false when the launcher would keep
+// the feature walk (cs = 1 or 128 rows a CTA or more).
+static bool check_column_split(const std::vector<int64_t>& widths, bool swiglu, int kb_total,
+                               int sms, RowTiling* out) {
+  Params p;
+  p.tp = (int)widths.size();
+  p.act = swiglu ? TP_ACT_SWIGLU : TP_ACT_GELU_ERF;
+  p.fo[0] = 0;
+  for (int i = 0; i < p.tp; ++i) p.fo[i + 1] = p.fo[i] + widths[i];
+  p.feat_total = p.fo[p.tp];
+  p.kb_total = kb_total;
+  const int64_t units = (p.feat_total + SK_GRAIN - 1) / SK_GRAIN;
+  const int64_t grid = units < sms ? units : sms;
+  const int64_t max_range = (units + grid - 1) / grid * SK_GRAIN;
+  const int64_t walk_cap = 256 < max_range ? 256 : max_range;
+  if ((swiglu ? 2 * walk_cap : walk_cap) >= 128) return false;
+  const int wf = swiglu ? SK_BN / 2 : SK_BN;
+  const RowTiling ct =
+      choose_row_tiling(p.feat_total, kb_total, kb_total / 32, sms, 8, 1, kResident, wf);
+  *out = ct;
+  if (ct.cs < 2) return false;
+  bool ok = false;
+  [&] {
+    CHECK(ct.tiles == (p.feat_total + wf - 1) / wf && ct.cs <= 8 && 32 * ct.cs <= kb_total &&
+              ct.tiles <= kResident[ct.cs],
+          "%lld tiles x %d", (long long)ct.tiles, ct.cs);
+    p.cs = ct.cs;
+    p.tile_cap = wf;
+    const int tile_rows = swiglu ? 2 * wf : wf;
+    int64_t expect = 0;
+    for (int64_t tile = 0; tile < ct.tiles; ++tile) {
+      int next_kb = 0;
+      for (int rank = 0; rank < ct.cs; ++rank) {
+        const int64_t block = tile * ct.cs + rank;
+        int64_t f0, f1;
+        column_split_range_of(p, block, f0, f1);
+        CHECK(f0 == expect && f1 > f0 && f1 - f0 <= wf, "cluster %lld range [%lld, %lld)",
+              (long long)tile, (long long)f0, (long long)f1);
+        int kb0, kb1;
+        split_kb_range(p, rank, kb0, kb1);
+        CHECK(kb0 == next_kb && kb1 > kb0, "rank %d k-range [%d, %d)", rank, kb0, kb1);
+        next_kb = kb1;
+        walk_tiles(p, widths, swiglu, tile_rows, f0, f1);
+        if (fails) return;
+        // partial-sum slots: feature offset in the range (+ wf for up rows)
+        for (int64_t f = f0; f < f1;) {
+          const Tile t = column_tile(p, f, f1);
+          for (int i = 0; i < t.n; ++i) {
+            const int64_t fl0 = p.fo[t.pc[i].shard] + t.pc[i].loc - f0;
+            CHECK(fl0 >= 0 && fl0 + t.pc[i].c <= f1 - f0, "piece slot [%lld, %lld)",
+                  (long long)fl0, (long long)(fl0 + t.pc[i].c));
+            CHECK(fl0 + t.pc[i].c + (swiglu ? wf : 0) <= SK_BN + 4, "beyond the buffer row");
+          }
+        }
+        if (rank == ct.cs - 1) expect = f1;
+      }
+      CHECK(next_kb == kb_total, "ranks end at k-block %d of %d", next_kb, kb_total);
+    }
+    CHECK(expect == p.feat_total, "clusters end at %lld of %lld", (long long)expect,
+          (long long)p.feat_total);
+    ok = true;
+  }();
+  return ok;
+}
 
 // The launchers' choice for n_out outputs and tp shards of kbs k-blocks:
 // bf16 kernel (cluster unit 1) and FP8 kernels (unit tp, one shard per CTA).
@@ -212,6 +295,35 @@ int main() {
   check_column({1}, false, 256, sms);
   check_column({16}, true, 256, sms);
   for (int tp = 1; tp <= 8; ++tp) check_column(std::vector<int64_t>(tp, 130 * tp + 7), true, 256, sms);
+  // column side with K split: the QKV projection of the 70B attention at
+  // tp 4 ((64 + 16) heads x 128 / 4 = 2560 per shard, K 8192): 40 tiles of
+  // 256 x 3 CTAs; small and ragged shapes; the choice equals tp = 1's
+  {
+    RowTiling q;
+    const bool split = check_column_split(std::vector<int64_t>(4, 2560), false, 128, sms, &q);
+    if (!(split && q.cs == 3 && q.tiles == 40)) {
+      std::printf("FAIL: QKV split %d: %lld tiles x %d\n", (int)split, (long long)q.tiles, q.cs);
+      ++fails;
+    }
+  }
+  const std::vector<std::vector<int64_t>> split_shapes = {
+      {2560, 2560, 2560, 2560}, {1025, 1025, 1025, 1025}, {5, 4}, {300, 200, 500},
+      {136, 8, 256, 40}, {200, 200, 200}, {576, 576}, {250, 250, 250, 250}, {1}, {16},
+      {2050, 2050}, {1000, 1000, 1000}, {3000}, {100, 100, 100, 100, 100, 100, 100, 100}};
+  for (const auto& w : split_shapes)
+    for (bool sw : {false, true})
+      for (int kb : {1, 2, 3, 16, 63, 64, 96, 128, 448}) {
+        RowTiling a, one;
+        int64_t total = 0;
+        for (int64_t x : w) total += x;
+        const bool sa = check_column_split(w, sw, kb, sms, &a);
+        const bool s1 = check_column_split({total}, sw, kb, sms, &one);
+        if (sa != s1 || (sa && (a.cs != one.cs || a.tiles != one.tiles))) {
+          std::printf("FAIL: split choice depends on the shards (%lld features)\n",
+                      (long long)total);
+          ++fails;
+        }
+      }
   // row side: bf16 kernel cs = min(8, 148 / tiles) (capped by the k-blocks);
   // FP8 kernels cs = tp x j
   check_row(8192, 4, 112, 256, 4, true);
