@@ -45,8 +45,12 @@
  *     to the output dtype (round to nearest even for bf16).  fp32 inputs use
  *     fp32 FMA on CUDA cores (no TF32).
  *   - Determinism: the summation order of a column-parallel output depends
- *     only on (M, K, dtype, act), never on N or tp, so a sharded run is
- *     bit-identical to the same call with tp = 1.
+ *     only on (M, K, the total output count N, dtype, act) and the device's
+ *     SM count, never on tp or the shard widths, so a sharded run is
+ *     bit-identical to the same call with tp = 1.  (Decode-shaped calls whose
+ *     outputs would give each SM fewer than 128 weight rows split K over a
+ *     cluster and add the partials in a fixed order; whether they do depends
+ *     on N, K and M.)
  */
 #ifndef TPLA_H
 #define TPLA_H

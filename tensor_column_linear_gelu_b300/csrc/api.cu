@@ -1,9 +1,11 @@
 // api.cu -- the C-ABI entry points of include/tpla.h: argument validation
 // (before any launch; on error nothing is written) and kernel dispatch.
 //
-// Dispatch keys on (M, K, dtype, act) only -- never on N or tp -- so a
-// column-parallel call computes every output with the same kernel and the
-// same summation order whatever the shard count.
+// Dispatch keys on (M, K, dtype, act) only -- never on N or tp -- and the
+// kernels' own tilings never on tp (the decode kernel's K split depends on
+// the total output count, K and M), so a column-parallel call computes every
+// output with the same kernel and the same summation order whatever the
+// shard count.
 #include <cstdint>
 #include <cstring>
 #include <map>
