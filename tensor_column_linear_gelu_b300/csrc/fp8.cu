@@ -67,9 +67,12 @@ __global__ void __launch_bounds__(QTHREADS) quantize_fp8_rows_kernel(
 // Warps per block: one for a single token -- 32-thread blocks spread the
 // warps evenly over the SMs (one-token SwiGLU FFN, tp 4: column 81 against
 // 83 us, step 128 against 130 us; 2- and 4-warp blocks were slower than 8);
-// eight for more tokens.
-template <int MT>
-constexpr int warps_of() { return MT == 1 ? 1 : 8; }
+// eight for more tokens.  A one-token row split takes two warps per output
+// group, each walking half of the shards (RSPLIT below).
+template <int MT, bool ROW>
+constexpr bool row_halves() { return ROW && MT == 1; }
+template <int MT, bool ROW>
+constexpr int warps_of() { return row_halves<MT, ROW>() ? 2 : (MT == 1 ? 1 : 8); }
 constexpr int E = 16;  // weights per 16-byte vector
 
 struct Fp8Params {
@@ -143,16 +146,23 @@ __device__ __forceinline__ void accumulate_fp8(float (&acc)[MT][NR], const uint8
 }
 
 template <int MT, int R, int U, int ACT, bool ROW>
-__global__ void __launch_bounds__(warps_of<MT>() * 32) gemv_fp8_kernel(const __grid_constant__ Fp8Params p) {
-  constexpr int kWarps = warps_of<MT>();
+__global__ void __launch_bounds__(warps_of<MT, ROW>() * 32) gemv_fp8_kernel(const __grid_constant__ Fp8Params p) {
+  constexpr int kWarps = warps_of<MT, ROW>();
+  // RSPLIT (one token, row split): the block's two warps take the same
+  // output group, warp h the shards [h*tp/2, (h+1)*tp/2); warp 0 adds warp
+  // 1's sums to its own (a fixed order) and stores.  Twice the warps stream
+  // the same bytes, so twice the loads are in flight.
+  constexpr bool RSPLIT = row_halves<MT, ROW>();
+  __shared__ float half_sum[RSPLIT ? 32 : 1];
   constexpr bool SW = (ACT == TP_ACT_SWIGLU);
   constexpr int NR = SW ? 2 * R : R;
   constexpr int64_t G = TP_GATE_UP_GROUP;
   static_assert(MT * R <= 32, "one lane stores one output");
 
   const int lane = threadIdx.x & 31;
-  const int64_t warp_global = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const int64_t warp_stride = (int64_t)gridDim.x * kWarps;
+  const int wib = threadIdx.x >> 5;  // warp in block
+  const int64_t warp_global = RSPLIT ? blockIdx.x : (int64_t)blockIdx.x * kWarps + wib;
+  const int64_t warp_stride = RSPLIT ? gridDim.x : (int64_t)gridDim.x * kWarps;
   const int64_t n_tasks = (p.n_out + R - 1) / R;
   const int64_t nvec = p.K / E;
   // The next kernel may start now.  (This kernel is launched in plain
@@ -192,8 +202,11 @@ __global__ void __launch_bounds__(warps_of<MT>() * 32) gemv_fp8_kernel(const __g
           accumulate_fp8<MT, NR, U>(acc, wr, p.X, p.ldx, p.M, m0, c0, nvec);
       } else {
         // each shard's lane partial is scaled by that shard's row scale, then
-        // added to the running sum (shard order 0..tp-1)
-        for (int i = 0; i < p.tp; ++i) {
+        // added to the running sum (shard order 0..tp-1; RSPLIT: within each
+        // half, then half 1's sum added to half 0's)
+        const int i0 = RSPLIT ? wib * p.tp / 2 : 0;
+        const int i1 = RSPLIT ? (wib + 1) * p.tp / 2 : p.tp;
+        for (int i = i0; i < i1; ++i) {
           const uint8_t* wr[NR];
           float part[MT][NR];
 #pragma unroll
@@ -228,12 +241,23 @@ __global__ void __launch_bounds__(warps_of<MT>() * 32) gemv_fp8_kernel(const __g
           acc[mm][r] = v;
         }
 
+      if constexpr (RSPLIT) {
+        if (wib == 1 && lane == 0) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) half_sum[r] = acc[0][r];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[0][r] += half_sum[r];
+        __syncthreads();  // half_sum is rewritten for the next output group
+      }
+
       // epilogue: lane (mm*R + r) finishes output (m0+mm, t*R+r)
 #pragma unroll
       for (int mm = 0; mm < MT; ++mm)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          if (lane != mm * R + r) continue;
+          if (lane != mm * R + r || (RSPLIT && wib != 0)) continue;
           const int64_t m = m0 + mm;
           const int64_t o = t * R + r;
           if (m >= p.M || o >= p.n_out) continue;
@@ -263,7 +287,7 @@ __global__ void __launch_bounds__(warps_of<MT>() * 32) gemv_fp8_kernel(const __g
 template <int MT, int R, int U, int ACT, bool ROW>
 tp_status prepare_fp8(const Fp8Params& gp, Launch* L) {
   auto kern = gemv_fp8_kernel<MT, R, U, ACT, ROW>;
-  constexpr int kWarps = warps_of<MT>();
+  constexpr int kWarps = warps_of<MT, ROW>();
   constexpr int kThreads = kWarps * 32;
   static int resident = 0;
   static std::once_flag once;
@@ -273,7 +297,7 @@ tp_status prepare_fp8(const Fp8Params& gp, Launch* L) {
     resident = std::max(b, 1);
   });
   const int64_t n_tasks = (gp.n_out + R - 1) / R;
-  const int64_t want = (n_tasks + kWarps - 1) / kWarps;
+  const int64_t want = row_halves<MT, ROW>() ? n_tasks : (n_tasks + kWarps - 1) / kWarps;
   L->kernel = reinterpret_cast<const void*>(kern);
   L->grid = dim3((unsigned)std::max<int64_t>(1, std::min(want, (int64_t)resident * sm_count())));
   L->block = dim3(kThreads);
